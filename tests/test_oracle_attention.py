@@ -1,0 +1,145 @@
+"""Pins of the oracle's attention (paper §3.1 Eq 1, §3.2 Eq 3 and Eq 6,
+§3.3 Eq 7) against numpy's softmax, exact identities and bounds (no GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+
+def _f(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .to(torch.float64).numpy()
+
+
+def _e4m3_val(c):
+    return torch.from_numpy(np.ascontiguousarray(c, np.uint8)).view(torch.float8_e4m3fn) \
+        .to(torch.float64).numpy()
+
+
+def _softmax_attention(q, k, v):
+    s = q @ k.T / np.sqrt(q.shape[1])
+    s -= s.max(1, keepdims=True)
+    p = np.exp(s)
+    return (p / p.sum(1, keepdims=True)) @ v
+
+
+@pytest.fixture(scope="module")
+def small():
+    q, k, v = synth.make_qkv(1, 1, 333, 128, 6, 2024)   # 333 keys: three tiles, ragged
+    return q[0, 0], k[0, 0], v[0, 0]
+
+
+def test_exact_matches_numpy_softmax(orc, small):
+    q, k, v = small
+    rows = np.arange(0, 333, 7)
+    ours = orc.attention_exact(q, k, v, rows)
+    ref = _softmax_attention(_f(q)[rows], _f(k), _f(v))
+    assert np.allclose(ours, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_permutation_invariance_eq3(orc, small):
+    q, k, v = small
+    perm = np.random.default_rng(1).permutation(333)
+    rows = np.arange(333)
+    a = orc.attention_exact(q, k, v, rows)
+    b = orc.attention_exact(q, k[perm], v[perm], rows)
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+@pytest.mark.parametrize("Bv", [128, 16, 100 - 36])
+def test_mean_restoration_eq6(orc, small, Bv):
+    """Eq 6 with exact exp and unquantised residual equals Eq 1 exactly."""
+    q, k, v = small
+    N = 333
+    perm = np.random.default_rng(2).permutation(N)
+    kp, vp = _f(k)[perm], _f(v)[perm]
+    nb = (N + Bv - 1) // Bv
+    mu = np.stack([vp[j * Bv:(j + 1) * Bv].mean(0) for j in range(nb)])
+    r = vp - np.repeat(mu, Bv, 0)[:N]
+    rows = np.arange(0, N, 5)
+    got = orc.attention_recurrence(_f(q), kp, r, mu, Bv, 0, rows)
+    ref = orc.attention_exact(q, k, v, rows)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_expcast_recurrence_output_bound(orc, small):
+    """Prop 3.1 / Eq 15 on the running-max recurrence: rows whose scores stay in
+    the normal range move by at most 3.64% of diam(V')."""
+    q, k, v = small
+    qf, kf, vf = _f(q) * 0.25, _f(k), _f(v)     # mild scores: no underflow tail
+    N, Bv = 333, 128
+    mu = np.zeros(((N + Bv - 1) // Bv, 128))
+    rows = np.arange(N)
+    exact = orc.attention_recurrence(qf, kf, vf, mu, Bv, 0, rows)
+    fast = orc.attention_recurrence(qf, kf, vf, mu, Bv, 1, rows)
+    s = qf @ kf.T / np.sqrt(128) * np.log2(np.e)
+    assert np.all(s - s.max(1, keepdims=True) >= -14)
+    lo, hi = vf.min(0), vf.max(0)
+    diam = np.linalg.norm(hi - lo)           # >= the largest row distance
+    err = np.linalg.norm(fast - exact, axis=1)
+    assert np.all(err <= 0.0364 * diam)
+    assert err.max() > 0                     # ExpCast does perturb
+
+
+@pytest.fixture(scope="module")
+def prep8(orc):
+    q, k, v = synth.make_qkv(1, 1, 700, 128, 8, 99)
+    p = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 5, 99)
+    return q[0, 0], k[0, 0], v[0, 0], p
+
+
+def test_attention8_is_the_recurrence_on_dequantised_operands(orc, prep8):
+    q, k, v, p = prep8
+    N, d = 700, 128
+    qd = _e4m3_val(p["qhat"][:N]) * np.repeat(p["sq"], 128)[:N, None]
+    kd = _e4m3_val(p["khat"][:N]) * np.repeat(p["sk"], 128)[:N, None]
+    rd = _e4m3_val(p["rhatT"][:, :N]).T * p["sv"][None, :]
+    mu = _f(p["mu"])
+    rows = np.arange(0, N, 3)
+    ref = orc.attention_recurrence(qd, kd, rd, mu, 128, 1, rows)
+    bits, got = orc.attention8(p, rows)
+    # mu enters attention8 as fp32(mu / sv) * sv: a relative 2^-24 rounding
+    assert np.max(np.abs(got - ref)) < 1e-6 * np.max(np.abs(ref))
+    gotb = _f(bits)
+    assert np.all(np.abs(gotb - got) <= np.abs(got) * 2.0 ** -8)
+
+
+def test_attention8_value_path_with_flat_scores(orc):
+    """q = 0: every score is 0, every byte is 120 (value 256), so the output is
+    the mean of the dequantised residual plus the restored block means."""
+    N = 500
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 3)
+    q0 = np.zeros_like(q[0, 0])
+    p = orc.prepare8(q0, k[0, 0], v[0, 0], 8, 3, 3)
+    _, got = orc.attention8(p, np.arange(0, N, 50))
+    vf = _f(v[0, 0])
+    R = vf[p["perm"]] - np.repeat(_f(p["mu"]), 128, 0)[:N]
+    tol = np.abs(R).mean(0) / 16 + p["sv"] * 2.0 ** -9
+    assert np.all(np.abs(got - vf.mean(0)[None, :]) <= tol[None, :] + 1e-9)
+
+
+def test_attention4_value_path_with_flat_scores(orc):
+    N = 500
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 4)
+    q0 = np.zeros_like(q[0, 0])
+    p = orc.prepare4(q0, k[0, 0], v[0, 0], 8, 3, 4)
+    _, got = orc.attention4(p, np.arange(0, N, 50))
+    vf = _f(v[0, 0])
+    gr = float(p["gr"][0])
+    scale = np.repeat(_e4m3_val(p["r4s"]), 16, 1)[:, :N] * gr        # per element step unit
+    tol = scale.mean(1)                                               # one E2M1 unit
+    assert np.all(np.abs(got - vf.mean(0)[None, :]) <= tol[None, :] + 1e-9)
+
+
+def test_quantised_attention_against_exact_report(orc, prep8):
+    q, k, v, p = prep8
+    rows = np.arange(0, 700, 11)
+    ex = orc.attention_exact(q, k, v, rows)
+    _, o8 = orc.attention8(p, rows)
+    p4 = orc.prepare4(q, k, v, 8, 5, 99)
+    _, o4 = orc.attention4(p4, rows)
+    e8 = np.linalg.norm(o8 - ex) / np.linalg.norm(ex)
+    e4 = np.linalg.norm(o4 - ex) / np.linalg.norm(ex)
+    print(f"rel L2 vs exact fp64: 8-bit {e8:.4f}, 4-bit {e4:.4f}")
+    assert e8 < 0.1 and e4 < 0.4
