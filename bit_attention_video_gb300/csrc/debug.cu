@@ -1,0 +1,211 @@
+// Test entry points: the ExpCast device function, the format encoders, and a
+// single-tile tcgen05 product with each operand layout the kernels rely on.
+#include "common.cuh"
+#include "expcast.cuh"
+
+namespace vca {
+namespace {
+
+__global__ void expcast_kernel(const float* acc, const float* a, const float* b, uint8_t* out,
+                               size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)expcast_code(acc[i], a[i], b[i]);
+}
+
+__global__ void encode_kernel(const float* x, uint8_t* e4, uint8_t* e2, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    e4[i] = f32_to_e4m3(x[i]);
+    e2[i] = f32x2_to_e2m1x2(x[i], 0.0f) & 0x0F;
+  }
+}
+
+// Byte offset of element (r, k) of a K-major tile with 128-byte swizzle;
+// `ebytes` bytes per element, 128/ebytes elements per swizzle atom column,
+// atom columns `atom_stride` bytes apart.
+__device__ uint32_t off_k_sw128(int r, int k, int ebytes, uint32_t atom_stride) {
+  const int per_atom = 128 / ebytes;
+  const int atom = k / per_atom, kb = (k % per_atom) * ebytes;
+  return atom * atom_stride + r * 128 + ((((kb >> 4) ^ (r & 7)) << 4) | (kb & 15));
+}
+// MN-major, 128-byte swizzle, 16-bit elements: MN chunks of 64 `lbo` bytes
+// apart, K rows of 128 bytes, 8-row groups of 1024 bytes.
+__device__ uint32_t off_mn_sw128(int n, int k, uint32_t lbo) {
+  const int chunk = n / 64, nb = (n % 64) * 2;
+  return chunk * lbo + k * 128 + ((((nb >> 4) ^ (k & 7)) << 4) | (nb & 15));
+}
+// K-major, no swizzle: 8-row x 16-byte core matrices, LBO along K, SBO along M/N.
+__device__ uint32_t off_k_plain(int r, int k, int ebytes, uint32_t lbo, uint32_t sbo) {
+  const int kb = k * ebytes;
+  return (r / 8) * sbo + (kb / 16) * lbo + (r % 8) * 16 + (kb % 16);
+}
+
+constexpr uint32_t kDbgSmem = 200 * 1024;
+__device__ int g_debug_status;  // wait-timeout bits of the layout test kernel
+
+__global__ void __launch_bounds__(128, 1)
+    mma_kernel(int mode, const uint8_t* a, const uint8_t* b, float* d) {
+  int* status = &g_debug_status;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t A = base, B = base + 65536;  // operand regions
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+  }
+  for (uint32_t i = tid; i < kDbgSmem / 4; i += 128) reinterpret_cast<uint32_t*>(sm)[i] = 0;
+  __syncthreads();
+
+  const uint16_t* a16 = reinterpret_cast<const uint16_t*>(a);
+  const uint16_t* b16 = reinterpret_cast<const uint16_t*>(b);
+  // operands into shared memory
+  if (mode == 0 || mode == 5 || mode == 6) {  // FP8 K-major swizzled, K = 128
+    for (int i = tid; i < 128 * 128; i += 128) {
+      int r = i / 128, k = i % 128;
+      if (mode != 5) sm[(A - base) + off_k_sw128(r, k, 1, 16384)] = a[i];
+      sm[(B - base) + off_k_sw128(r, k, 1, 16384)] = b[i];
+    }
+  }
+  if (mode == 1 || mode == 4) {  // BF16 K-major swizzled, K = 128 (two atom columns)
+    for (int i = tid; i < 128 * 128; i += 128) {
+      int r = i / 128, k = i % 128;
+      if (mode == 1) *reinterpret_cast<uint16_t*>(sm + (A - base) + off_k_sw128(r, k, 2, 16384)) = a16[i];
+      *reinterpret_cast<uint16_t*>(sm + (B - base) + off_k_sw128(r, k, 2, 16384)) = b16[i];
+    }
+  }
+  if (mode == 2) {  // A K-major swizzled K = 64; B MN-major swizzled
+    for (int i = tid; i < 128 * 64; i += 128) {
+      int r = i / 64, k = i % 64;
+      *reinterpret_cast<uint16_t*>(sm + (A - base) + off_k_sw128(r, k, 2, 16384)) = a16[i];
+      *reinterpret_cast<uint16_t*>(sm + (B - base) + off_mn_sw128(r, k, 8192)) = b16[i];
+    }
+  }
+  if (mode == 3 || mode == 6) {  // BF16 K-major no swizzle, K = 16
+    const uint16_t* as = mode == 6 ? reinterpret_cast<const uint16_t*>(a + 128 * 128) : a16;
+    const uint16_t* bs = mode == 6 ? reinterpret_cast<const uint16_t*>(b + 128 * 128) : b16;
+    const uint32_t A2 = mode == 6 ? A + 32768 : A, B2 = mode == 6 ? B + 32768 : B;
+    for (int i = tid; i < 128 * 16; i += 128) {
+      int r = i / 16, k = i % 16;
+      *reinterpret_cast<uint16_t*>(sm + (A2 - base) + off_k_plain(r, k, 2, 128, 256)) = as[i];
+      *reinterpret_cast<uint16_t*>(sm + (B2 - base) + off_k_plain(r, k, 2, 128, 256)) = bs[i];
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  // A operand in tensor memory (columns 128..): row r in lane r, K packed
+  // little-endian into 32-bit columns (2 bf16 or 4 fp8 per column).
+  if (mode == 4 || mode == 5) {
+    const int r = warp * 32 + lane;
+    const int ncol = mode == 4 ? 64 : 32;
+    for (int c0 = 0; c0 < ncol; c0 += 32) {
+      uint32_t w[32];
+      for (int c = 0; c < 32; ++c) {
+        if (mode == 4)
+          w[c] = (uint32_t)a16[r * 128 + 2 * (c0 + c)] |
+                 ((uint32_t)a16[r * 128 + 2 * (c0 + c) + 1] << 16);
+        else
+          w[c] = *reinterpret_cast<const uint32_t*>(a + r * 128 + 4 * (c0 + c));
+      }
+      tmem_st32(tmem + lane_base + 128 + c0, w);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (tid == 0) {
+    const uint32_t i8 = idesc_f8(128, 128), i16 = idesc_bf16(128, 128),
+                   i16mn = idesc_bf16(128, 128, true);
+    if (mode == 0 || mode == 6)
+      for (int s = 0; s < 4; ++s)
+        mma_f8_ss(tmem, desc_k_sw128(A + 32 * s), desc_k_sw128(B + 32 * s), i8, s > 0);
+    if (mode == 1)
+      for (int s = 0; s < 8; ++s) {
+        uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
+        mma_f16_ss(tmem, desc_k_sw128(A + o), desc_k_sw128(B + o), i16, s > 0);
+      }
+    if (mode == 2)
+      for (int s = 0; s < 4; ++s)
+        mma_f16_ss(tmem, desc_k_sw128(A + 32 * s), make_desc(B + 2048 * s, 8192, 1024, 2), i16mn,
+                   s > 0);
+    if (mode == 3)
+      mma_f16_ss(tmem, desc_k_plain(A, 128, 256), desc_k_plain(B, 128, 256), i16, 0);
+    if (mode == 6)
+      mma_f16_ss(tmem, desc_k_plain(A + 32768, 128, 256), desc_k_plain(B + 32768, 128, 256), i16,
+                 1);
+    if (mode == 4)
+      for (int s = 0; s < 8; ++s) {
+        uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
+        mma_f16_ts(tmem, tmem + 128 + 8 * s, desc_k_sw128(B + o), i16, s > 0);
+      }
+    if (mode == 5)
+      for (int s = 0; s < 4; ++s)
+        mma_f8_ts(tmem, tmem + 128 + 8 * s, desc_k_sw128(B + 32 * s), i8, s > 0);
+    mma_commit(smem_u32(&bar));
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, status);
+  tc_fence_after();
+  if (ok) {
+    const int r = warp * 32 + lane;
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + c0, v);
+      tmem_ld_wait();
+      for (int c = 0; c < 32; ++c) d[r * 128 + c0 + c] = __uint_as_float(v[c]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+}  // namespace vca
+
+using namespace vca;
+
+extern "C" int vca_debug_expcast(const float* acc, const float* a, const float* b, uint8_t* out,
+                                 size_t n, vca_stream_t stream) {
+  if (n == 0) return VCA_OK;
+  if (!acc || !a || !b || !out) return VCA_ERR_INVALID_ARG;
+  int blocks = (int)std::min<size_t>((n + 255) / 256, 152 * 16);
+  expcast_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(acc, a, b, out, n);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+extern "C" int vca_debug_encode(const float* x, uint8_t* e4, uint8_t* e2, size_t n,
+                                vca_stream_t stream) {
+  if (n == 0) return VCA_OK;
+  if (!x || !e4 || !e2) return VCA_ERR_INVALID_ARG;
+  int blocks = (int)std::min<size_t>((n + 255) / 256, 152 * 16);
+  encode_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(x, e4, e2, n);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+extern "C" int vca_debug_mma(int mode, const void* a, const void* b, float* d,
+                             vca_stream_t stream) {
+  if (mode < 0 || mode > 6 || !a || !b || !d) return VCA_ERR_INVALID_ARG;
+  if (cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kDbgSmem + 1024) != cudaSuccess)
+    return VCA_ERR_CUDA;
+  mma_kernel<<<1, 128, kDbgSmem + 1024, (cudaStream_t)stream>>>(
+      mode, (const uint8_t*)a, (const uint8_t*)b, d);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}

@@ -1,0 +1,620 @@
+// V-Smooth preprocessing kernels (paper §3.2 Eq 3-4, §3.4 "Fused
+// preprocessing", Appx B).  All are memory-bound passes except the k-means
+// assignment.  Every floating-point step that decides a stored code is a
+// single IEEE operation written with an explicit-rounding intrinsic, and every
+// floating-point sum has a fixed order, so codes, scales and means are
+// reproducible bit for bit.
+#include "common.cuh"
+#include "prep.h"
+
+namespace vca {
+namespace {
+
+__device__ __forceinline__ bool prep_skip(const int* status) {
+  return *(volatile const int*)status != 0;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide max over blockDim.x threads (multiple of 32, <= 1024).
+__device__ float block_max(float v, float* red) {
+  v = warp_max(v);
+  const int w = threadIdx.x / 32, nw = blockDim.x / 32;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float m = 0.0f;
+  for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+// Per-block fp32 E4M3 scale: amax / 448, or 1 for an all-zero block.
+__device__ __forceinline__ float e4m3_scale(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+// SplitMix64 (Steele, Lea & Flood 2014).
+__device__ __forceinline__ uint64_t splitmix64_next(uint64_t& s) {
+  s += 0x9E3779B97F4A7C15ull;
+  uint64_t z = s;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// ---------------------------------------------------------------------------
+// state header / reuse check
+// ---------------------------------------------------------------------------
+__global__ void header_kernel(uint32_t* hdr, int* status, int B, int H, int N, int d, int k,
+                              int bits, int reuse) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  if (reuse) {
+    const bool match = hdr[0] == kStateMagic && hdr[1] == (uint32_t)B && hdr[2] == (uint32_t)H &&
+                       hdr[3] == (uint32_t)N && hdr[4] == (uint32_t)d && hdr[5] == (uint32_t)k &&
+                       hdr[6] == (uint32_t)bits && hdr[7] == 1u;
+    *status = match ? 0 : kStatNoPerm;
+    if (match) hdr[8] = 0;  // operands being rewritten
+    return;
+  }
+  hdr[0] = kStateMagic;
+  hdr[1] = B; hdr[2] = H; hdr[3] = N; hdr[4] = d; hdr[5] = k; hdr[6] = bits;
+  hdr[7] = 0;  // permutation cached
+  hdr[8] = 0;  // operands ready
+  *status = 0;
+}
+
+__global__ void header_done_kernel(uint32_t* hdr, const int* status, int set_perm) {
+  if (threadIdx.x != 0 || blockIdx.x != 0 || prep_skip(status)) return;
+  if (set_perm) hdr[7] = 1;
+  hdr[8] = 1;
+}
+
+__global__ void zero_kernel(uint32_t* p, size_t words) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < words;
+       i += (size_t)gridDim.x * blockDim.x)
+    p[i] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// k-means on the int8 feature grid (paper §3.2 "Value-guided permutation")
+// ---------------------------------------------------------------------------
+// grid (chunks, BH): max |V| of each head, as the uint bits of a non-negative float.
+__global__ void head_amax_kernel(const uint16_t* v, uint32_t* amax_bits, size_t per_head,
+                                 const int* status) {
+  __shared__ float red[32];
+  if (prep_skip(status)) return;
+  const size_t bh = blockIdx.y;
+  const uint4* src = reinterpret_cast<const uint4*>(v + bh * per_head);
+  const size_t n16 = per_head / 8;
+  float m = 0.0f;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
+       i += (size_t)gridDim.x * blockDim.x) {
+    uint4 w = src[i];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      m = fmaxf(m, fabsf(__uint_as_float(ws[e] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(ws[e] & 0xFFFF0000u)));
+    }
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
+}
+
+// x = clamp(RNE(v / s), -127, 127), s = amax / 127 (1 if amax = 0).
+__global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, float* grid_scale,
+                                int8_t* x, size_t per_head, const int* status) {
+  if (prep_skip(status)) return;
+  const size_t bh = blockIdx.y;
+  const float amax = __uint_as_float(amax_bits[bh]);
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) grid_scale[bh] = s;
+  const uint4* src = reinterpret_cast<const uint4*>(v + bh * per_head);
+  uint2* dst = reinterpret_cast<uint2*>(x + bh * per_head);
+  const size_t n8 = per_head / 8;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    uint4 w = src[i];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[2] = {0, 0};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t bits = (e & 1) ? (ws[e / 2] & 0xFFFF0000u) : (ws[e / 2] << 16);
+      int q = __float2int_rn(__fdiv_rn(__uint_as_float(bits), s));
+      q = max(-127, min(127, q));
+      out[e / 4] |= ((uint32_t)(q & 0xFF)) << (8 * (e % 4));
+    }
+    dst[i] = make_uint2(out[0], out[1]);
+  }
+}
+
+// grid BH, 128 threads: initial centroids = features of k distinct tokens drawn
+// by SplitMix64 from seed ^ (0x9E3779B97F4A7C15 * (bh + 1)); zero the sums.
+__global__ void kmeans_init_kernel(const int8_t* x, int8_t* cent, int32_t* sums, int32_t* counts,
+                                   uint64_t seed, int N, int k, int d, int* status) {
+  __shared__ int32_t idx[256];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x;
+  if (threadIdx.x == 0) {
+    uint64_t st = seed ^ (0x9E3779B97F4A7C15ull * (uint64_t)(bh + 1));
+    int have = 0;
+    // k <= N distinct draws; the bound only guards against a corrupted k
+    for (long long tries = 0; have < k && tries < (1ll << 26); ++tries) {
+      const int32_t cand = (int32_t)(splitmix64_next(st) % (uint64_t)N);
+      bool dup = false;
+      for (int i = 0; i < have; ++i) dup |= (idx[i] == cand);
+      if (!dup) idx[have++] = cand;
+    }
+    if (have < k) atomicOr(status, kStatBadArg);
+  }
+  __syncthreads();
+  for (int m = 0; m < k; ++m)
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      cent[((size_t)bh * k + m) * d + c] = x[((size_t)bh * N + idx[m]) * d + c];
+      sums[((size_t)bh * k + m) * d + c] = 0;
+    }
+  for (int m = threadIdx.x; m < k; m += blockDim.x) counts[(size_t)bh * k + m] = 0;
+}
+
+// grid (ceil(N / kAssignTokens), BH), 256 threads.  Phase 1: every token's
+// nearest centroid by exact integer distance ||c||^2 - 2 x.c (the token's own
+// norm is common to all centroids), lowest index on ties.  Phase 2: the tile's
+// per-cluster channel sums in shared memory (one thread per channel, tokens in
+// order, no atomics), then one global atomic add per (cluster, channel).
+constexpr int kAssignTokens = 1024;
+// Shared words of the assign kernel for k clusters and `groups` accumulators.
+inline size_t assign_smem_bytes(int k, int groups) {
+  return (size_t)(k * 32 + k + kAssignTokens + groups * (k * 128 + k)) * 4;
+}
+__global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, const int8_t* cent,
+                                                            int32_t* labels, int32_t* sums,
+                                                            int32_t* counts, int N, int k,
+                                                            int groups, const int* status) {
+  extern __shared__ int32_t sm[];
+  int32_t* cw = sm;                      // centroids as packed int8x4 words [k][32]
+  int32_t* cnorm = cw + k * 32;          // [k]
+  int32_t* lab = cnorm + k;              // [kAssignTokens]
+  int32_t* acc = lab + kAssignTokens;    // [groups][k*128 sums + k counts]
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, t0 = blockIdx.x * kAssignTokens;
+  const int ntok = min(kAssignTokens, N - t0);
+  const int32_t* cg = reinterpret_cast<const int32_t*>(cent + (size_t)bh * k * 128);
+  for (int i = threadIdx.x; i < k * 32; i += blockDim.x) cw[i] = cg[i];
+  for (int i = threadIdx.x; i < groups * (k * 128 + k); i += blockDim.x) acc[i] = 0;
+  __syncthreads();
+  for (int m = threadIdx.x; m < k; m += blockDim.x) {
+    int32_t n2 = 0;
+    for (int w = 0; w < 32; ++w) n2 = __dp4a(cw[m * 32 + w], cw[m * 32 + w], n2);
+    cnorm[m] = n2;
+  }
+  __syncthreads();
+  const int8_t* xh = x + ((size_t)bh * N + t0) * 128;
+  for (int t = threadIdx.x; t < ntok; t += blockDim.x) {
+    int32_t xw[32];
+    const int4* row = reinterpret_cast<const int4*>(xh + (size_t)t * 128);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      int4 v = row[q];
+      xw[4 * q] = v.x; xw[4 * q + 1] = v.y; xw[4 * q + 2] = v.z; xw[4 * q + 3] = v.w;
+    }
+    int best = 0x7FFFFFFF, bestm = 0;
+    for (int m = 0; m < k; ++m) {
+      int32_t dot = 0;
+#pragma unroll
+      for (int w = 0; w < 32; ++w) dot = __dp4a(xw[w], cw[m * 32 + w], dot);
+      const int dist = cnorm[m] - 2 * dot;
+      if (dist < best) { best = dist; bestm = m; }
+    }
+    lab[t] = bestm;
+    labels[(size_t)bh * N + t0 + t] = bestm;
+  }
+  __syncthreads();
+  // phase 2: `groups` groups of 128 threads (one per channel), each over a
+  // contiguous share of the tile's tokens, in token order
+  const int g = threadIdx.x / 128, c = threadIdx.x % 128;
+  if (g < groups) {
+    int32_t* a = acc + g * (k * 128 + k);
+    const int share = (ntok + groups - 1) / groups, lo = g * share, hi = min(ntok, lo + share);
+    for (int t = lo; t < hi; ++t) {
+      const int z = lab[t];
+      a[z * 128 + c] += (int32_t)xh[(size_t)t * 128 + c];
+      if (c == 0) a[k * 128 + z] += 1;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < k * 128 + k; i += blockDim.x) {
+    int32_t s = 0;
+    for (int gg = 0; gg < groups; ++gg) s += acc[gg * (k * 128 + k) + i];
+    if (s != 0) {
+      if (i < k * 128) atomicAdd(&sums[(size_t)bh * k * 128 + i], s);
+      else atomicAdd(&counts[(size_t)bh * k + (i - k * 128)], s);
+    }
+  }
+}
+
+// Round-half-even of s / n (n > 0) in exact integer arithmetic.
+__device__ __forceinline__ int div_rne(int s, int n) {
+  int q = s / n, r = s % n;
+  if (r < 0) { q -= 1; r += n; }
+  if (2 * r > n || (2 * r == n && (q & 1))) q += 1;
+  return q;
+}
+
+// grid (BH, k), 128 threads: centroid = RNE integer mean of its members; an
+// empty cluster keeps its centroid.  Clears the sums for the next iteration.
+__global__ void kmeans_update_kernel(int8_t* cent, int32_t* sums, int32_t* counts, int k,
+                                     const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x, m = blockIdx.y, c = threadIdx.x;
+  const size_t o = ((size_t)bh * k + m) * 128 + c;
+  const int n = counts[(size_t)bh * k + m];
+  if (n > 0) cent[o] = (int8_t)div_rne(sums[o], n);
+  sums[o] = 0;
+  __syncthreads();
+  if (c == 0) counts[(size_t)bh * k + m] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Stable counting sort of the labels: pi = argsort(z) (paper Eq 3)
+// ---------------------------------------------------------------------------
+constexpr int kSortChunk = 2048;
+// grid (chunks, BH): hist[bh][label][chunk]
+__global__ void sort_hist_kernel(const int32_t* labels, int32_t* hist, int N, int k, int nchunk,
+                                 const int* status) {
+  __shared__ int32_t h[256];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, ch = blockIdx.x;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const int t0 = ch * kSortChunk, t1 = min(N, t0 + kSortChunk);
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x)
+    atomicAdd(&h[labels[(size_t)bh * N + t]], 1);
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += blockDim.x)
+    hist[((size_t)bh * k + i) * nchunk + ch] = h[i];
+}
+
+// grid BH, 256 threads: hist -> exclusive offsets in (label, chunk) order.
+__global__ void sort_scan_kernel(int32_t* hist, int k, int nchunk, const int* status) {
+  __shared__ int32_t tot[256];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x;
+  int32_t* hh = hist + (size_t)bh * k * nchunk;
+  for (int m = threadIdx.x; m < k; m += blockDim.x) {
+    int s = 0;
+    for (int c = 0; c < nchunk; ++c) s += hh[m * nchunk + c];
+    tot[m] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int m = 0; m < k; ++m) { const int t = tot[m]; tot[m] = run; run += t; }
+  }
+  __syncthreads();
+  for (int m = threadIdx.x; m < k; m += blockDim.x) {
+    int run = tot[m];
+    for (int c = 0; c < nchunk; ++c) { const int t = hh[m * nchunk + c]; hh[m * nchunk + c] = run; run += t; }
+  }
+}
+
+// grid (chunks, BH), 256 threads: stable scatter.  Tokens of a chunk are taken
+// in rounds of 256 in order; within a round a token's rank among equal labels
+// comes from warp match masks and per-warp counts.
+__global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* labels,
+                                                           const int32_t* offs, int32_t* perm,
+                                                           int N, int k, int nchunk,
+                                                           const int* status) {
+  __shared__ int32_t base[256];
+  __shared__ int32_t wcnt[8][256];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, ch = blockIdx.x, w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int m = threadIdx.x; m < k; m += blockDim.x)
+    base[m] = offs[((size_t)bh * k + m) * nchunk + ch];
+  const int t0 = ch * kSortChunk, t1 = min(N, t0 + kSortChunk);
+  for (int r0 = t0; r0 < t1; r0 += 256) {
+    for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int t = r0 + threadIdx.x;
+    const bool valid = t < t1;
+    const int z = valid ? labels[(size_t)bh * N + t] : -1 - lane;  // unique per invalid lane
+    const unsigned same = __match_any_sync(0xffffffffu, z);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (valid && rank == 0) wcnt[w][z] = __popc(same);
+    __syncthreads();
+    if (valid) {
+      int pos = base[z] + rank;
+      for (int ww = 0; ww < w; ++ww) pos += wcnt[ww][z];
+      perm[(size_t)bh * N + pos] = t;
+    }
+    __syncthreads();
+    for (int m = threadIdx.x; m < k; m += blockDim.x) {
+      int s = 0;
+      for (int ww = 0; ww < 8; ++ww) s += wcnt[ww][m];
+      base[m] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Quantizers (8-bit)
+// ---------------------------------------------------------------------------
+// Load 64 consecutive bf16 of a row into fp32.
+__device__ __forceinline__ void load64(const uint16_t* src, float (&f)[64]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 w = s[q];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[q * 8 + 2 * e] = __uint_as_float(ws[e] << 16);
+      f[q * 8 + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+    }
+  }
+}
+__device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64], float s) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = q * 16 + e * 4;
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(f[i + 2], s), __fdiv_rn(f[i + 3], s));
+      w[e] = lo | (hi << 16);
+    }
+    d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// grid (nb, BH), 256 threads: per 128-token block, sQ = amax / 448 and
+// Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ...
+__global__ void __launch_bounds__(256) quant_q8_kernel(const uint16_t* q, uint8_t* qhat, float* sq,
+                                                       int N, int Npad, int nb, const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
+  float f[64];
+  if (row < N) load64(q + ((size_t)bh * N + row) * 128 + h * 64, f);
+  else
+    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  float m = 0.0f;
+  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
+  const float s = e4m3_scale(block_max(m, red));
+  if (threadIdx.x == 0) sq[(size_t)bh * nb + j] = s;
+  store64_e4m3(qhat + ((size_t)bh * Npad + row) * 128 + h * 64, f, s);
+}
+
+// Fixed pairwise tree over 128 values: v[r] += v[r + 64], then + 32, ... .
+__device__ __forceinline__ float tree128(float (&v)[128]) {
+#pragma unroll
+  for (int s = 64; s >= 1; s >>= 1)
+#pragma unroll
+    for (int r = 0; r < s; ++r) v[r] = __fadd_rn(v[r], v[r + s]);
+  return v[0];
+}
+
+// grid (nb, BH), 128 threads (one per channel): fp32 tree sum of each block of
+// the original key order.
+__global__ void __launch_bounds__(128) key_block_sum_kernel(const uint16_t* k, float* ksum, int N,
+                                                            int nb, const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  float v[128];
+#pragma unroll
+  for (int r = 0; r < 128; ++r) {
+    const int row = j * 128 + r;
+    v[r] = row < N ? bf16_bits_to_f32(k[((size_t)bh * N + row) * 128 + c]) : 0.0f;
+  }
+  ksum[((size_t)bh * nb + j) * 128 + c] = tree128(v);
+}
+
+// grid BH, 128 threads: kbar = bf16(fp32(sum of block sums in block order, in
+// fp64, / N)).
+__global__ void key_mean_kernel(const float* ksum, uint16_t* kbar, int N, int nb,
+                                const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x, c = threadIdx.x;
+  double t = 0.0;
+  for (int j = 0; j < nb; ++j) t = __dadd_rn(t, (double)ksum[((size_t)bh * nb + j) * 128 + c]);
+  kbar[(size_t)bh * 128 + c] = f32_to_bf16_bits(__double2float_rn(__ddiv_rn(t, (double)N)));
+}
+
+// grid (nb, BH), 256 threads: K' = K[pi] - kbar, per-block E4M3.
+__global__ void __launch_bounds__(256) quant_k8_kernel(const uint16_t* k, const int32_t* perm,
+                                                       const uint16_t* kbar, uint8_t* khat,
+                                                       float* sk, int N, int Npad, int nb,
+                                                       const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
+  float f[64];
+  if (row < N) {
+    const int src = perm[(size_t)bh * N + row];
+    load64(k + ((size_t)bh * N + src) * 128 + h * 64, f);
+    const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
+    for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
+  } else {
+    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  }
+  float m = 0.0f;
+  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
+  const float s = e4m3_scale(block_max(m, red));
+  if (threadIdx.x == 0) sk[(size_t)bh * nb + j] = s;
+  store64_e4m3(khat + ((size_t)bh * Npad + row) * 128 + h * 64, f, s);
+}
+
+// Gather one channel of one permuted block (zero rows past N).
+__device__ __forceinline__ void gather_channel(const uint16_t* v, const int32_t* perm, int bh,
+                                               int j, int c, int N, float (&x)[128]) {
+#pragma unroll
+  for (int r = 0; r < 128; ++r) {
+    const int row = j * 128 + r;
+    x[r] = row < N ? bf16_bits_to_f32(v[((size_t)bh * N + perm[(size_t)bh * N + row]) * 128 + c])
+                   : 0.0f;
+  }
+}
+
+// grid (nb, BH), 128 threads (one per channel): block mean (Eq 4) of V' =
+// V[pi]: fp32 tree sum / n_j, rounded to bf16; residual channel maxima.
+__global__ void __launch_bounds__(128) vpass1_kernel(const uint16_t* v, const int32_t* perm,
+                                                     uint16_t* mu, float* vamax, int N, int nb,
+                                                     const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  const int nj = min(128, N - j * 128);
+  float x[128];
+  gather_channel(v, perm, bh, j, c, N, x);
+  const float mean = __fdiv_rn(tree128(x), (float)nj);
+  const uint16_t m16 = f32_to_bf16_bits(mean);
+  const float mf = bf16_bits_to_f32(m16);
+  gather_channel(v, perm, bh, j, c, N, x);  // the tree overwrote x; re-read (cache hits)
+  float amax = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 128; ++r)
+    if (r < nj) amax = fmaxf(amax, fabsf(__fsub_rn(x[r], mf)));
+  mu[((size_t)bh * nb + j) * 128 + c] = m16;
+  vamax[((size_t)bh * nb + j) * 128 + c] = amax;
+}
+
+// grid BH, 128 threads: sv = max over blocks / 448; mutilde = mu / sv; the
+// mean operand of the restoration MMA: per block a 128 (channel) x 16 bf16
+// K-major tile without swizzle whose K columns 0, 1, 2 hold (hi, hi, lo) of
+// mutilde (the A side supplies (r_hi, r_lo, r_hi)).
+__global__ void vreduce_kernel(const float* vamax, const uint16_t* mu, float* sv, float* mutilde,
+                               uint8_t* mside, int nb, const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x, c = threadIdx.x;
+  float m = 0.0f;
+  for (int j = 0; j < nb; ++j) m = fmaxf(m, vamax[((size_t)bh * nb + j) * 128 + c]);
+  const float s = e4m3_scale(m);
+  sv[(size_t)bh * 128 + c] = s;
+  for (int j = 0; j < nb; ++j) {
+    const size_t o = ((size_t)bh * nb + j) * 128 + c;
+    const float mt = __fdiv_rn(bf16_bits_to_f32(mu[o]), s);
+    mutilde[o] = mt;
+    const uint16_t hi = f32_to_bf16_bits(mt);
+    const uint16_t lo = f32_to_bf16_bits(__fsub_rn(mt, bf16_bits_to_f32(hi)));
+    uint8_t* tile = mside + ((size_t)bh * nb + j) * kSideTileBytes;
+    // element (n = c, k) at (c/8)*256 + (k/8)*128 + (c%8)*16 + (k%8)*2
+    uint4* p0 = reinterpret_cast<uint4*>(tile + (c / 8) * 256 + (c % 8) * 16);
+    uint4* p1 = reinterpret_cast<uint4*>(tile + (c / 8) * 256 + 128 + (c % 8) * 16);
+    *p0 = make_uint4((uint32_t)hi | ((uint32_t)hi << 16), (uint32_t)lo, 0u, 0u);
+    *p1 = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// grid (nb, BH), 128 threads (one per channel): R = V' - mu, R^ = E4M3(R / sv)
+// written transposed (tokens fastest).
+__global__ void __launch_bounds__(128) vpass2_kernel(const uint16_t* v, const int32_t* perm,
+                                                     const uint16_t* mu, const float* sv,
+                                                     uint8_t* rhatT, int N, int Npad, int nb,
+                                                     const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  float x[128];
+  gather_channel(v, perm, bh, j, c, N, x);
+  const float mf = bf16_bits_to_f32(mu[((size_t)bh * nb + j) * 128 + c]);
+  const float s = sv[(size_t)bh * 128 + c];
+  uint4* dst = reinterpret_cast<uint4*>(rhatT + ((size_t)bh * 128 + c) * Npad + (size_t)j * 128);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = q * 16 + e * 4 + u;
+        y[u] = (j * 128 + r < N) ? __fdiv_rn(__fsub_rn(x[r], mf), s) : 0.0f;
+      }
+      w[e] = (uint32_t)f32x2_to_e4m3x2(y[0], y[1]) | ((uint32_t)f32x2_to_e4m3x2(y[2], y[3]) << 16);
+    }
+    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+inline int grid_chunks(size_t work, int per_block, int cap) {
+  return (int)std::max<size_t>(1, std::min<size_t>((work + per_block - 1) / per_block, cap));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host: the preparation chain
+// ---------------------------------------------------------------------------
+int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
+  const int BH = a.B * a.H, N = a.N, nb = a.nb, Npad = a.Npad, k = a.k;
+  const size_t per_head = (size_t)N * 128;
+  uint8_t* S = a.state;
+  const vca_state_layout& L = a.L;
+  int* status = reinterpret_cast<int*>(S + L.status);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(S + L.header);
+  const uint16_t* q = a.q;
+  const uint16_t* kk = a.k_in;
+  const uint16_t* v = a.v;
+  int32_t* labels = reinterpret_cast<int32_t*>(S + L.labels);
+  int32_t* perm = reinterpret_cast<int32_t*>(S + L.perm);
+
+  header_kernel<<<1, 32, 0, st>>>(hdr, status, a.B, a.H, N, 128, k, 8, a.reuse);
+  if (!a.reuse) {
+    uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + L.grid);
+    float* gscale = reinterpret_cast<float*>(S + L.grid) + BH;
+    int8_t* x = reinterpret_cast<int8_t*>(S + L.features);
+    int8_t* cent = reinterpret_cast<int8_t*>(S + L.centroids);
+    int32_t* sums = reinterpret_cast<int32_t*>(S + L.sums);
+    int32_t* counts = sums + (size_t)BH * k * 128;
+    zero_kernel<<<1, 256, 0, st>>>(amax_bits, BH);
+    const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
+    head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, per_head, status);
+    features_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
+    kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
+    const int groups = k <= 96 ? 2 : 1;
+    const size_t asmem = assign_smem_bytes(k, groups);
+    cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)asmem);
+    const int tiles = (N + kAssignTokens - 1) / kAssignTokens;
+    for (int it = 0; it < a.iters; ++it) {
+      kmeans_assign_kernel<<<dim3(tiles, BH), 256, asmem, st>>>(x, cent, labels, sums, counts, N,
+                                                                k, groups, status);
+      kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
+    }
+    // stable counting sort; the k-means sums buffer is reused for the histogram
+    const int nchunk = (N + kSortChunk - 1) / kSortChunk;
+    int32_t* hist = reinterpret_cast<int32_t*>(S + L.ksum);  // [BH][k][nchunk] fits in ksum
+    sort_hist_kernel<<<dim3(nchunk, BH), 256, 0, st>>>(labels, hist, N, k, nchunk, status);
+    sort_scan_kernel<<<BH, 256, 0, st>>>(hist, k, nchunk, status);
+    sort_scatter_kernel<<<dim3(nchunk, BH), 256, 0, st>>>(labels, hist, perm, N, k, nchunk,
+                                                          status);
+  }
+  uint8_t* qhat = S + L.qhat;
+  float* sq = reinterpret_cast<float*>(S + L.sq);
+  uint8_t* khat = S + L.khat;
+  float* sk = reinterpret_cast<float*>(S + L.sk);
+  uint16_t* kbar = reinterpret_cast<uint16_t*>(S + L.kbar);
+  float* ksum = reinterpret_cast<float*>(S + L.ksum);
+  uint8_t* rhatT = S + L.rhatT;
+  float* sv = reinterpret_cast<float*>(S + L.sv);
+  uint16_t* mu = reinterpret_cast<uint16_t*>(S + L.mu);
+  float* mut = reinterpret_cast<float*>(S + L.mutilde);
+  uint8_t* mside = S + L.mside;
+  float* vamax = reinterpret_cast<float*>(S + L.vamax);
+  quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
+  key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
+  key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
+  quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
+  vpass1_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  vreduce_kernel<<<BH, 128, 0, st>>>(vamax, mu, sv, mut, mside, nb, status);
+  vpass2_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, sv, rhatT, N, Npad, nb, status);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+}  // namespace vca

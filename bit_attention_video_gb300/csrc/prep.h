@@ -1,0 +1,45 @@
+// Internal interfaces of the VC-Attention library: state-blob layout, the
+// arguments of the preparation chain and the kernel launchers.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/vca.h"
+
+namespace vca {
+
+constexpr uint32_t kStateMagic = 0x31414356u;  // "VCA1"
+constexpr uint32_t kSideTileBytes = 128 * 16 * 2;  // bf16 128 x 16 mean operand per block
+constexpr uint32_t kTileBytes = 128 * 128;         // one 128 x 128 E4M3 tile
+
+// Header words (uint32): magic, B, H, N, d, k, bits, perm cached, operands ready.
+
+// Computes the blob layout; returns VCA_OK or an argument error.
+int compute_layout(int B, int H, int N, int d, int k, int bits, vca_state_layout* L);
+
+struct PrepArgs {
+  const uint16_t* q;
+  const uint16_t* k_in;
+  const uint16_t* v;
+  int B, H, N, nb, Npad, k, iters, reuse;
+  uint64_t seed;
+  uint8_t* state;
+  vca_state_layout L;
+};
+
+int launch_prepare8(const PrepArgs& a, cudaStream_t st);
+int launch_prepare4(const PrepArgs& a, cudaStream_t st);
+int launch_attention_fp8(uint8_t* state, const vca_state_layout& L, int B, int H, int N, void* o,
+                         cudaStream_t st);
+int launch_attention_nvfp4(uint8_t* state, const vca_state_layout& L, int B, int H, int N,
+                           void* o, cudaStream_t st);
+int launch_attention_bf16(const void* q, const void* k, const void* v, int B, int H, int N,
+                          void* o, int* status, cudaStream_t st);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// 2-D tensor of `elem_bytes`-byte elements: inner extent `dim0`, `dim1` rows of
+// `row_bytes` bytes, box (box0, box1), 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
+                  uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1);
+
+}  // namespace vca

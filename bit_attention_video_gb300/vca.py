@@ -1,0 +1,234 @@
+"""Thin Python binding of the VC-Attention C ABI (``include/vca.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libvca.so``.  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing the import of a function fails
+loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvca.so")
+_lib = None
+
+VCA_OK = 0
+STATUS_NAMES = {0: "VCA_OK", -1: "VCA_ERR_INVALID_ARG", -2: "VCA_ERR_UNSUPPORTED",
+                -3: "VCA_ERR_CUDA", -4: "VCA_ERR_BUFFER_TOO_SMALL",
+                -5: "VCA_ERR_NO_CACHED_PERM", -6: "VCA_ERR_TIMEOUT",
+                -7: "VCA_ERR_STATE_MISMATCH"}
+DEFAULT_ITERS = 10
+DEFAULT_SEED = 0
+
+
+class VcaError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class StateLayout(C.Structure):
+    _fields_ = [(n, C.c_uint64) for n in (
+        "total_bytes", "header", "status", "labels", "perm", "centroids", "grid", "features",
+        "sums", "qhat", "sq", "khat", "sk", "kbar", "ksum", "rhatT", "sv", "mu", "mutilde",
+        "mside", "vamax", "q4", "q4s", "k4", "k4s", "r4T", "r4s", "g4")]
+
+
+def lib():
+    """Load libvca.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run bit_attention_video_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        P, I, S, U64 = C.c_void_p, C.c_int, C.c_size_t, C.c_uint64
+        L.vca_state_bytes.restype = S
+        L.vca_state_bytes.argtypes = [I] * 6
+        L.vca_state_layout_get.restype = I
+        L.vca_state_layout_get.argtypes = [I] * 6 + [C.POINTER(StateLayout)]
+        L.vca_vsmooth_prepare.restype = I
+        L.vca_vsmooth_prepare.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, P, S, P]
+        for fn in ("vca_attention_fp8", "vca_attention_nvfp4"):
+            getattr(L, fn).restype = I
+            getattr(L, fn).argtypes = [P, S, I, I, I, I, P, P]
+        L.vca_attention_bf16_ref.restype = I
+        L.vca_attention_bf16_ref.argtypes = [P, P, P, I, I, I, I, P, P, P]
+        L.vca_get_status.restype = I
+        L.vca_get_status.argtypes = [P, P, P]
+        L.vca_status_string.restype = C.c_char_p
+        L.vca_status_string.argtypes = [I]
+        L.vca_debug_expcast.restype = I
+        L.vca_debug_expcast.argtypes = [P, P, P, P, S, P]
+        L.vca_debug_encode.restype = I
+        L.vca_debug_encode.argtypes = [P, P, P, S, P]
+        L.vca_debug_mma.restype = I
+        L.vca_debug_mma.argtypes = [I, P, P, P, P]
+        _lib = L
+    return _lib
+
+
+def _check(fn, rc):
+    if rc != VCA_OK:
+        raise VcaError(fn, rc)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype=None):
+    assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    if dtype is not None:
+        assert t.dtype == dtype, f"expected {dtype}, got {t.dtype}"
+    return C.c_void_p(t.data_ptr())
+
+
+# ----------------------------------------------------------------------------
+def state_bytes(B, H, N, d, k_clusters, bits) -> int:
+    return lib().vca_state_bytes(B, H, N, d, k_clusters, bits)
+
+
+def state_layout(B, H, N, d, k_clusters, bits) -> StateLayout:
+    L = StateLayout()
+    _check("vca_state_layout_get", lib().vca_state_layout_get(B, H, N, d, k_clusters, bits,
+                                                              C.byref(L)))
+    return L
+
+
+def alloc_state(B, H, N, d, k_clusters, bits, device="cuda") -> torch.Tensor:
+    n = state_bytes(B, H, N, d, k_clusters, bits)
+    if n == 0:
+        raise VcaError("vca_state_bytes", -1)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def vsmooth_prepare(q, k, v, k_clusters, state, reuse_perm=False, bits=8,
+                    iters=DEFAULT_ITERS, seed=DEFAULT_SEED, stream=None):
+    B, H, N, d = q.shape
+    _check("vca_vsmooth_prepare", lib().vca_vsmooth_prepare(
+        _dev(q, torch.bfloat16), _dev(k, torch.bfloat16), _dev(v, torch.bfloat16), B, H, N, d,
+        k_clusters, int(reuse_perm), bits, iters, seed, _dev(state, torch.uint8),
+        state.numel(), _stream(stream)))
+
+
+def attention_fp8(state, shape, out, stream=None):
+    B, H, N, d = shape
+    _check("vca_attention_fp8", lib().vca_attention_fp8(
+        _dev(state, torch.uint8), state.numel(), B, H, N, d, _dev(out, torch.bfloat16),
+        _stream(stream)))
+
+
+def attention_nvfp4(state, shape, out, stream=None):
+    B, H, N, d = shape
+    _check("vca_attention_nvfp4", lib().vca_attention_nvfp4(
+        _dev(state, torch.uint8), state.numel(), B, H, N, d, _dev(out, torch.bfloat16),
+        _stream(stream)))
+
+
+def attention_bf16_ref(q, k, v, out, status=None, stream=None):
+    B, H, N, d = q.shape
+    _check("vca_attention_bf16_ref", lib().vca_attention_bf16_ref(
+        _dev(q, torch.bfloat16), _dev(k, torch.bfloat16), _dev(v, torch.bfloat16), B, H, N, d,
+        _dev(out, torch.bfloat16), _dev(status, torch.int32) if status is not None else None,
+        _stream(stream)))
+
+
+def get_status(state=None, status_word=None, stream=None) -> int:
+    """Synchronise the stream and read-and-clear the device status word."""
+    return lib().vca_get_status(_dev(state) if state is not None else None,
+                                _dev(status_word) if status_word is not None else None,
+                                _stream(stream))
+
+
+def debug_expcast(acc, a, b, out, stream=None):
+    _check("vca_debug_expcast", lib().vca_debug_expcast(
+        _dev(acc, torch.float32), _dev(a, torch.float32), _dev(b, torch.float32),
+        _dev(out, torch.uint8), acc.numel(), _stream(stream)))
+
+
+def debug_encode(x, out_e4m3, out_e2m1, stream=None):
+    _check("vca_debug_encode", lib().vca_debug_encode(
+        _dev(x, torch.float32), _dev(out_e4m3, torch.uint8), _dev(out_e2m1, torch.uint8),
+        x.numel(), _stream(stream)))
+
+
+def debug_mma(mode, a, b, d, stream=None):
+    _check("vca_debug_mma", lib().vca_debug_mma(mode, _dev(a), _dev(b), _dev(d, torch.float32),
+                                                _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
+    """Typed views of the arrays of a prepared state blob (for inspection)."""
+    B, H, N, d = shape
+    L = state_layout(B, H, N, d, k_clusters, bits)
+    BH, nb = B * H, (N + 127) // 128
+    Npad = nb * 128
+
+    def v(off, n, dtype, shp):
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return state[off:off + nbytes].view(dtype).view(*shp)
+
+    out = dict(
+        labels=v(L.labels, BH * N, torch.int32, (BH, N)),
+        perm=v(L.perm, BH * N, torch.int32, (BH, N)),
+        centroids=v(L.centroids, BH * k_clusters * d, torch.int8, (BH, k_clusters, d)),
+        kbar=v(L.kbar, BH * d, torch.int16, (BH, d)),
+        mu=v(L.mu, BH * nb * d, torch.int16, (BH, nb, d)),
+        mside=v(L.mside, BH * nb * 2048, torch.int16, (BH, nb, 2048)),
+        status=v(L.status, 1, torch.int32, (1,)),
+    )
+    if bits == 8:
+        out.update(
+            qhat=v(L.qhat, BH * Npad * d, torch.uint8, (BH, Npad, d)),
+            sq=v(L.sq, BH * nb, torch.float32, (BH, nb)),
+            khat=v(L.khat, BH * Npad * d, torch.uint8, (BH, Npad, d)),
+            sk=v(L.sk, BH * nb, torch.float32, (BH, nb)),
+            rhatT=v(L.rhatT, BH * d * Npad, torch.uint8, (BH, d, Npad)),
+            sv=v(L.sv, BH * d, torch.float32, (BH, d)),
+            mutilde=v(L.mutilde, BH * nb * d, torch.float32, (BH, nb, d)),
+        )
+    else:
+        out.update(
+            q4=v(L.q4, BH * Npad * d // 2, torch.uint8, (BH, Npad, d // 2)),
+            q4s=v(L.q4s, BH * Npad * d // 16, torch.uint8, (BH, Npad, d // 16)),
+            k4=v(L.k4, BH * Npad * d // 2, torch.uint8, (BH, Npad, d // 2)),
+            k4s=v(L.k4s, BH * Npad * d // 16, torch.uint8, (BH, Npad, d // 16)),
+            r4T=v(L.r4T, BH * d * Npad // 2, torch.uint8, (BH, d, Npad // 2)),
+            r4s=v(L.r4s, BH * d * Npad // 16, torch.uint8, (BH, d, Npad // 16)),
+            g4=v(L.g4, BH * 4, torch.float32, (BH, 4)),
+        )
+    return out
+
+
+class VCAttention:
+    """Convenience wrapper: owns a state blob for one problem shape."""
+
+    def __init__(self, B, H, N, d=128, k_clusters=64, bits=8, iters=DEFAULT_ITERS,
+                 seed=DEFAULT_SEED, device="cuda"):
+        self.shape = (B, H, N, d)
+        self.k, self.bits, self.iters, self.seed = k_clusters, bits, iters, seed
+        self.state = alloc_state(B, H, N, d, k_clusters, bits, device)
+
+    def prepare(self, q, k, v, reuse_perm=False, stream=None):
+        vsmooth_prepare(q, k, v, self.k, self.state, reuse_perm, self.bits, self.iters,
+                        self.seed, stream)
+
+    def attention(self, out, stream=None):
+        fn = attention_fp8 if self.bits == 8 else attention_nvfp4
+        fn(self.state, self.shape, out, stream)
+
+    def __call__(self, q, k, v, out=None, reuse_perm=False, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        self.prepare(q, k, v, reuse_perm, stream)
+        self.attention(out, stream)
+        return out
+
+    def status(self, stream=None) -> int:
+        return get_status(self.state, None, stream)

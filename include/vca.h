@@ -1,0 +1,174 @@
+/*
+ * vca.h — C ABI of the VC-Attention library for GB300 (sm_103a).
+ *
+ * VC-Attention ("VC-Attention: Value Smoothing and Softmax Casting for
+ * Low-bit Attention", arXiv 2609.15810) computes non-causal attention
+ * O = softmax(Q K^T / sqrt(d)) V with low-bit operands:
+ *   - V-Smooth (§3.2): per (batch, head) a k-means over value tokens gives
+ *     labels z and the stable permutation pi = argsort(z) (Eq 3); keys and
+ *     values are gathered by pi, each 128-row block mean mu_j is subtracted
+ *     (Eq 4) and only the residual is quantised.  Q and K are quantised to
+ *     E4M3 with one scale per 128-token block.
+ *   - The fused attention (§3.3, Eq 1, Eq 6, Eq 7): FP8 QK^T and PV on the
+ *     tensor cores, ExpCast-FP8 probability bytes, online mean restoration.
+ *
+ * Conventions for every function below
+ *   - Tensors Q, K, V, O are bf16, shape [B, H, N, d], contiguous row-major,
+ *     d fastest.  Device pointers must be 16-byte aligned.
+ *   - All memory is caller-owned.  The library never allocates, frees or
+ *     synchronises, except vca_get_status, which synchronises `stream`.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are returned synchronously, before any
+ *     launch; a launch failure returns VCA_ERR_CUDA.  Data-dependent failures
+ *     (a cached permutation that does not match, a device-side wait that
+ *     expired) are recorded in the state blob's status word and reported by
+ *     vca_get_status.
+ *   - d must be 128.  1 <= k_clusters <= min(N, 256).  N >= 1.
+ */
+#ifndef VCA_H
+#define VCA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vca_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  VCA_OK = 0,
+  VCA_ERR_INVALID_ARG = -1,      /* null pointer, bad shape, misaligned pointer */
+  VCA_ERR_UNSUPPORTED = -2,      /* d != 128, bits not 8 or 4, k out of range */
+  VCA_ERR_CUDA = -3,             /* a CUDA call or launch failed */
+  VCA_ERR_BUFFER_TOO_SMALL = -4, /* state_bytes < vca_state_bytes(...) */
+  VCA_ERR_NO_CACHED_PERM = -5,   /* reuse_perm=1 but the blob holds no matching permutation */
+  VCA_ERR_TIMEOUT = -6,          /* a device-side pipeline wait gave up (no hang) */
+  VCA_ERR_STATE_MISMATCH = -7    /* the blob was prepared for another shape or bit width */
+} vca_status;
+
+#define VCA_DEFAULT_ITERS 10
+#define VCA_DEFAULT_SEED 0ull
+#define VCA_BLOCK_ROWS 128 /* B_v: the hardware block of the block means (paper §3.2, Eq 4) */
+
+/* Offsets (bytes from the start of the state blob) of every array the
+ * preparation writes, for inspection and tests.  nb = ceil(N/128) blocks,
+ * Npad = 128*nb, BH = B*H.  An offset of 0 means "absent for this bit width". */
+typedef struct {
+  uint64_t total_bytes;
+  uint64_t header;    /* 256 B: shape, bit width, flags */
+  uint64_t status;    /* int32 status word (device side) */
+  uint64_t labels;    /* int32 [BH][N]  k-means label z of each token (last assignment) */
+  uint64_t perm;      /* int32 [BH][N]  pi: permuted row i holds source token perm[i] */
+  uint64_t centroids; /* int8  [BH][k][d] centroids on the int8 feature grid */
+  uint64_t grid;      /* fp32  [BH] per-head feature grid scale (and scratch) */
+  uint64_t features;  /* int8  [BH][N][d] k-means features (scratch) */
+  uint64_t sums;      /* int32 [BH][k][d] + counts int32 [BH][k] (scratch) */
+  uint64_t qhat;      /* e4m3  [BH][Npad][d] */
+  uint64_t sq;        /* fp32  [BH][nb]    Q block scales */
+  uint64_t khat;      /* e4m3  [BH][Npad][d] permuted, centred keys */
+  uint64_t sk;        /* fp32  [BH][nb]    K' block scales */
+  uint64_t kbar;      /* bf16  [BH][d]     key channel mean */
+  uint64_t ksum;      /* fp32  [BH][nb][d] per-block key sums (scratch) */
+  uint64_t rhatT;     /* e4m3  [BH][d][Npad] residual codes, tokens fastest */
+  uint64_t sv;        /* fp32  [BH][d]     per-channel residual scales */
+  uint64_t mu;        /* bf16  [BH][nb][d] block means (unscaled) */
+  uint64_t mutilde;   /* fp32  [BH][nb][d] mu / sv */
+  uint64_t mside;     /* bf16  [BH][nb][128*16] mean operand of the restoration MMA */
+  uint64_t vamax;     /* fp32  [BH][nb][d] per-block residual channel maxima (scratch) */
+  /* 4-bit (NVFP4) path */
+  uint64_t q4;        /* e2m1 packed [BH][Npad][d/2] */
+  uint64_t q4s;       /* ue4m3 [BH][Npad][d/16] */
+  uint64_t k4;        /* e2m1 packed [BH][Npad][d/2] */
+  uint64_t k4s;       /* ue4m3 [BH][Npad][d/16] */
+  uint64_t r4T;       /* e2m1 packed [BH][d][Npad/2] */
+  uint64_t r4s;       /* ue4m3 [BH][d][Npad/16] */
+  uint64_t g4;        /* fp32 [BH][4] global scales gq, gk, gr, - */
+} vca_state_layout;
+
+/* Size in bytes of the state blob for this problem (0 if the arguments are
+ * invalid).  The caller allocates it (any device allocation, 256-byte aligned). */
+size_t vca_state_bytes(int B, int H, int N, int d, int k_clusters, int bits);
+
+/* Fill `out` with the offsets of the state blob's arrays.  Returns VCA_OK or
+ * an argument error. */
+int vca_state_layout_get(int B, int H, int N, int d, int k_clusters, int bits,
+                         vca_state_layout* out);
+
+/* V-Smooth preprocessing (paper §3.2 Eq 3-4, §3.4 "Fused preprocessing",
+ * Appx B).  Reads q, k, v (bf16 [B,H,N,d], device) and writes every operand of
+ * the attention kernels into `state` (device, state_bytes >= vca_state_bytes).
+ *   k_clusters  k-means clusters per (b, h)
+ *   reuse_perm  0: run k-means (iters Lloyd iterations, seeded by `seed`) and
+ *               cache pi and the centroids in the blob; 1: skip grouping and
+ *               reuse the cached pi (paper §3.4 "Amortized grouping
+ *               schedule"); the blob must come from a call with the same
+ *               B, H, N, d, k_clusters and bits, else the status word gets
+ *               VCA_ERR_NO_CACHED_PERM and no operand is written.
+ *   bits        8 (E4M3 path) or 4 (NVFP4 path)
+ *   iters       >= 1 Lloyd iterations (VCA_DEFAULT_ITERS)
+ *   seed        k-means seed (VCA_DEFAULT_SEED); the initial centroids of head
+ *               (b,h) are k distinct tokens drawn by SplitMix64 from the state
+ *               seed ^ (0x9E3779B97F4A7C15 * (b*H + h + 1)).
+ * Clears the status word unless reuse fails. */
+int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                        int k_clusters, int reuse_perm, int bits, int iters, uint64_t seed,
+                        void* state, size_t state_bytes, vca_stream_t stream);
+
+/* 8-bit fused attention (paper §3.1 Eq 1, §3.2 Eq 6, §3.3 Eq 7): FP8 QK'^T
+ * and P R on tcgen05 tensor cores, ExpCast-FP8 probability bytes relative to
+ * the running row maximum, block means restored from the row sums in the same
+ * accumulator.  `state` must hold a bits=8 preparation of the same shape.
+ * Writes o (bf16 [B,H,N,d], device) in the original query order. */
+int vca_attention_fp8(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,
+                      vca_stream_t stream);
+
+/* 4-bit variant (paper §4.1 "Implementation", Appx A, Appx B): NVFP4 Q, K'
+ * and residual with E4M3 scales per 16 elements along each product's
+ * reduction dimension, conventional exponential, NVFP4 probabilities, means
+ * added unscaled.  `state` must hold a bits=4 preparation. */
+int vca_attention_nvfp4(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,
+                        vca_stream_t stream);
+
+/* BF16 reference attention on tcgen05 (the role BF16 FlashAttention-4 plays in
+ * paper §4.1 "Baselines"): exact-max online softmax with an fp32 exponential,
+ * bf16 probabilities.  q, k, v, o bf16 [B,H,N,d], device.  `status` is a
+ * device int32 that receives kernel-side failures (may be NULL). */
+int vca_attention_bf16_ref(const void* q, const void* k, const void* v, int B, int H, int N,
+                           int d, void* o, int* status, vca_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the status word of `state`
+ * (or of the int32 at `status_word` when state is NULL).  Returns VCA_OK or the
+ * first recorded error. */
+int vca_get_status(void* state, int* status_word, vca_stream_t stream);
+
+/* Human-readable name of a vca_status value. */
+const char* vca_status_string(int status);
+
+/* ---- test entry points (device buffers) ---- */
+
+/* ExpCast-FP8 device function on n inputs: out[i] = clip_[0,120](RNE(fma(a[i],
+ * acc[i], b[i]))) (paper §3.3 Eq 7 in the single-FMA form). */
+int vca_debug_expcast(const float* acc, const float* a, const float* b, uint8_t* out, size_t n,
+                      vca_stream_t stream);
+
+/* The device E4M3 and E2M1 encoders on n fp32 inputs (out_e2m1: one code per
+ * byte, low nibble). */
+int vca_debug_encode(const float* x, uint8_t* out_e4m3, uint8_t* out_e2m1, size_t n,
+                     vca_stream_t stream);
+
+/* One 128 x N tcgen05 product with the operand layouts the kernels use, for
+ * layout tests.  mode: 0 FP8 K-major 128B-swizzle (K=128); 1 BF16 K-major
+ * 128B-swizzle (K=128); 2 BF16 with B MN-major 128B-swizzle (K=64);
+ * 3 BF16 K-major no-swizzle (K=16); 4 BF16 with A in tensor memory (K=128);
+ * 5 FP8 with A in tensor memory (K=128); 6 mode 0 followed by mode 3 into the
+ * same accumulator.  a: [128][K] row-major (bytes per element as the mode's
+ * type; for mode 6, a holds the 128x128 FP8 A then the 128x16 BF16 A), b:
+ * [N][K] row-major likewise, d: fp32 [128][N]; N = 128. */
+int vca_debug_mma(int mode, const void* a, const void* b, float* d, vca_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VCA_H */

@@ -81,6 +81,10 @@ def _declare(L):
     L.orc_e2m1_decode.argtypes = [C.c_uint8]
     L.orc_e2m1_encode.restype = C.c_uint8
     L.orc_e2m1_encode.argtypes = [C.c_float]
+    L.orc_e4m3_encode_array.restype = None
+    L.orc_e4m3_encode_array.argtypes = [_P, _P, C.c_size_t]
+    L.orc_e2m1_encode_array.restype = None
+    L.orc_e2m1_encode_array.argtypes = [_P, _P, C.c_size_t]
     L.orc_expcast_code.restype = C.c_int
     L.orc_expcast_code.argtypes = [C.c_double]
     L.orc_expcast_code_f32.restype = C.c_int
@@ -137,6 +141,20 @@ def e4m3_encode(x) -> np.ndarray:
     L = lib()
     return np.array([L.orc_e4m3_encode(float(v)) for v in np.asarray(x, np.float32).ravel()],
                     dtype=np.uint8)
+
+
+def e4m3_encode_array(x) -> np.ndarray:
+    x = _c(x, np.float32).ravel()
+    out = np.zeros(x.size, np.uint8)
+    lib().orc_e4m3_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e2m1_encode_array(x) -> np.ndarray:
+    x = _c(x, np.float32).ravel()
+    out = np.zeros(x.size, np.uint8)
+    lib().orc_e2m1_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
 
 
 def e4m3_decode(c) -> np.ndarray:

@@ -164,6 +164,14 @@ uint8_t orc_e2m1_encode(float x) {
   return (uint8_t)(sign | c);
 }
 
+void orc_e4m3_encode_array(const float* x, uint8_t* out, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+
+void orc_e2m1_encode_array(const float* x, uint8_t* out, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode(x[i]);
+}
+
 // ---------------------------------------------------------------------------
 // ExpCast-FP8, paper §3.3 Eq 7
 // ---------------------------------------------------------------------------

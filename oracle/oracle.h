@@ -41,6 +41,9 @@ uint8_t  orc_e4m3_encode(float x);
  * RNE with saturation to +-6.  Pinned: format table and midpoint ties. */
 double   orc_e2m1_decode(uint8_t c);
 uint8_t  orc_e2m1_encode(float x);
+/* The same encoders over arrays. */
+void     orc_e4m3_encode_array(const float* x, uint8_t* out, size_t n);
+void     orc_e2m1_encode_array(const float* x, uint8_t* out, size_t n);
 
 /* ---------------- ExpCast-FP8 (paper §3.3 Eq 7, Appx C/D) ----------------- */
 /* Eq 7 literally, in fp64: c(u) = clip_[0,120](RNE(8(u+8)+56+beta)), beta=-0.35.

@@ -1,0 +1,88 @@
+"""GPU: the fused FP8 attention matches the CPU oracle's 8-bit VC-Attention
+within relative L2 2e-3 (the benchmark spec's tolerance), on full small problems,
+ragged lengths and sampled rows of larger ones; the BF16 reference kernel
+matches exact attention."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import bf16_f64, rel_l2, to_dev, to_np_u16
+
+pytestmark = pytest.mark.gpu
+TOL8 = 2e-3
+
+
+def run_fp8(q, k, v, kc, iters, seed):
+    from bit_attention_video_gb300 import vca
+    B, H, N, d = q.shape
+    att = vca.VCAttention(B, H, N, d, k_clusters=kc, bits=8, iters=iters, seed=seed)
+    out = att(to_dev(q), to_dev(k), to_dev(v))
+    st = att.status()
+    return to_np_u16(out), st
+
+
+@pytest.mark.parametrize("B,H,N,C,kc,iters", [
+    (1, 1, 1024, 16, 16, 10),
+    (1, 2, 1000, 16, 16, 4),
+    (2, 1, 300, 4, 8, 3),
+    (1, 1, 129, 4, 4, 2),
+    (1, 1, 1, 1, 1, 1),
+    (1, 3, 200, 8, 8, 2),
+])
+def test_fp8_attention_matches_oracle(orc, B, H, N, C, kc, iters):
+    seed = 0xBEEF + N
+    q, k, v = synth.make_qkv(B, H, N, 128, C, seed)
+    got, st = run_fp8(q, k, v, kc, iters, seed)
+    assert st == 0
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(H):
+            p = orc.prepare8(q[b, h], k[b, h], v[b, h], kc, iters, seed, b=b, h=h, H=H)
+            _, ref = orc.attention8(p, rows)
+            err = rel_l2(bf16_f64(got[b, h]), ref)
+            assert err <= TOL8, f"(b={b},h={h}) relative L2 {err:.3e}"
+
+
+def test_fp8_attention_h8_sampled_rows(orc):
+    w = synth.CONFIGS["h8"]
+    q, k, v = synth.make(w)
+    got, st = run_fp8(q, k, v, w.k, 10, w.seed)
+    assert st == 0
+    rng = np.random.default_rng(3)
+    for h in (1, 6):
+        rows = np.sort(rng.choice(w.N, 96, replace=False))
+        p = orc.prepare8(q[0, h], k[0, h], v[0, h], w.k, 10, w.seed, b=0, h=h, H=w.H)
+        _, ref = orc.attention8(p, rows)
+        err = rel_l2(bf16_f64(got[0, h][rows]), ref)
+        ex = orc.attention_exact(q[0, h], k[0, h], v[0, h], rows[:16])
+        print(f"h{h}: rel L2 vs oracle {err:.2e}, vs exact fp64 {rel_l2(bf16_f64(got[0, h][rows[:16]]), ex):.3e}")
+        assert err <= TOL8
+
+
+def test_fp8_attention_rejects_mismatched_state():
+    from bit_attention_video_gb300 import vca
+    q, k, v = synth.make_qkv(1, 1, 300, 128, 4, 1)
+    att = vca.VCAttention(1, 1, 300, 128, k_clusters=4, iters=2)
+    att.prepare(to_dev(q), to_dev(k), to_dev(v))
+    assert att.status() == 0
+    out = torch.empty(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
+    vca.attention_fp8(att.state, (1, 1, 256, 128), out)       # prepared for N = 300
+    assert vca.get_status(att.state) == -7
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1024), (1, 2, 1000), (2, 1, 129)])
+def test_bf16_reference_matches_exact(orc, B, H, N):
+    from bit_attention_video_gb300 import vca
+    q, k, v = synth.make_qkv(B, H, N, 128, 8, 77)
+    out = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vca.attention_bf16_ref(to_dev(q), to_dev(k), to_dev(v), out, status)
+    assert vca.get_status(None, status) == 0
+    got = to_np_u16(out)
+    rows = np.arange(0, N, 3)
+    for b in range(B):
+        for h in range(H):
+            ref = orc.attention_exact(q[b, h], k[b, h], v[b, h], rows)
+            err = rel_l2(bf16_f64(got[b, h][rows]), ref)
+            assert err <= 8e-3, f"(b={b},h={h}) relative L2 {err:.3e}"

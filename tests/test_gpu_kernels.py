@@ -1,0 +1,114 @@
+"""GPU: the ExpCast device function and the format encoders are bit-exact with
+the oracle; every tcgen05 operand layout the kernels use multiplies correctly."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def V():
+    from bit_attention_video_gb300 import vca
+    vca.lib()
+    return vca
+
+
+def test_expcast_device_function_bit_exact(V, orc):
+    rng = np.random.default_rng(11)
+    n = 1 << 20
+    a = rng.uniform(0.01, 3.0, n).astype(np.float32)
+    acc = rng.uniform(-400, 400, n).astype(np.float32)
+    M = (a * np.float32(400) * rng.uniform(0.5, 1.0, n).astype(np.float32)).astype(np.float32)
+    b = (np.float32(119.65) - M).astype(np.float32)
+    # exact rounding ties of fma(a, acc, b): a = 1, acc = k + 0.5 - b
+    k = rng.integers(-5, 125, 4096)
+    a[:4096] = 1.0
+    b[:4096] = np.float32(0.0)
+    acc[:4096] = (k + 0.5).astype(np.float32)
+    acc[4096:4099] = [np.nan, -np.inf, np.inf]
+    ref = orc.expcast_f32(acc, a, b)
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    V.debug_expcast(torch.from_numpy(acc).cuda(), torch.from_numpy(a).cuda(),
+                    torch.from_numpy(b).cuda(), out)
+    got = out.cpu().numpy()
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first at {bad[:5]}: {got[bad[:5]]} vs {ref[bad[:5]]}"
+
+
+def test_encoders_bit_exact(V, orc):
+    # every 40503rd bit pattern (~106k), random values, every E4M3 / E2M1
+    # midpoint and its two float neighbours
+    pats = np.arange(0, 1 << 32, 40503, dtype=np.uint64).astype(np.uint32)
+    rng = np.random.default_rng(12)
+    vals = [pats.view(np.float32),
+            rng.standard_normal(1 << 20).astype(np.float32) * np.float32(50),
+            rng.standard_normal(1 << 18).astype(np.float32) * np.float32(0.01)]
+    e4 = orc.e4m3_decode(np.arange(127))
+    e2 = orc.e2m1_decode(np.arange(8))
+    for grid in (e4, e2):
+        mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+        for m in (mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))):
+            vals += [m, -m]
+    x = np.concatenate(vals).astype(np.float32)
+    x = x[~np.isnan(x)]
+    o4 = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    o2 = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    V.debug_encode(torch.from_numpy(x).cuda(), o4, o2)
+    g4, g2 = o4.cpu().numpy(), o2.cpu().numpy()
+    r4 = orc.e4m3_encode_array(x)
+    r2 = orc.e2m1_encode_array(x)
+    assert np.array_equal(g4, r4), f"e4m3: {np.sum(g4 != r4)} mismatches at {x[g4 != r4][:5]}"
+    assert np.array_equal(g2, r2), f"e2m1: {np.sum(g2 != r2)} mismatches at {x[g2 != r2][:5]}"
+
+
+def _e4m3_small(rng, shape):
+    # exactly representable small values so products and sums are exact in fp32
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, -0.5, -1, -2, -3, 0.25, -0.25], np.float32)
+    return vals[rng.integers(0, vals.size, shape)]
+
+
+def _run_mma(V, mode, a, b):
+    d = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
+    V.debug_mma(mode, a.cuda(), b.cuda(), d)
+    torch.cuda.synchronize()
+    return d.cpu().numpy()
+
+
+@pytest.mark.parametrize("mode,K,kind", [(0, 128, "fp8"), (1, 128, "bf16"), (2, 64, "bf16"),
+                                         (3, 16, "bf16"), (4, 128, "bf16"), (5, 128, "fp8")])
+def test_mma_layouts(V, mode, K, kind):
+    rng = np.random.default_rng(100 + mode)
+    A = _e4m3_small(rng, (128, K))
+    Bm = _e4m3_small(rng, (128, K))
+    if kind == "fp8":
+        ta = torch.from_numpy(A).to(torch.float8_e4m3fn).view(torch.uint8)
+        tb = torch.from_numpy(Bm).to(torch.float8_e4m3fn).view(torch.uint8)
+    else:
+        ta = torch.from_numpy(A).to(torch.bfloat16)
+        tb = torch.from_numpy(Bm).to(torch.bfloat16)
+    got = _run_mma(V, mode, ta, tb)
+    ref = A.astype(np.float64) @ Bm.astype(np.float64).T
+    if not np.array_equal(got, ref):
+        diag = []
+        if mode in (4, 5):  # diagnose the packing order of the TMEM operand
+            g = 2 if mode == 4 else 4
+            Ap = A.reshape(128, -1, g)[:, :, ::-1].reshape(128, K)
+            diag.append(f"reversed packing matches: {np.array_equal(got, Ap @ Bm.T)}")
+        if mode == 2:
+            diag.append(f"B^T product matches: {np.array_equal(got, A @ Bm.reshape(K, 128))}")
+        pytest.fail(f"mode {mode}: max |err| {np.abs(got - ref).max()}, "
+                    f"{np.sum(got != ref)} mismatches; {'; '.join(diag)}")
+
+
+def test_mma_mixed_kinds_one_accumulator(V):
+    rng = np.random.default_rng(7)
+    A8, B8 = _e4m3_small(rng, (128, 128)), _e4m3_small(rng, (128, 128))
+    A16, B16 = _e4m3_small(rng, (128, 16)), _e4m3_small(rng, (128, 16))
+    ta = torch.cat([torch.from_numpy(A8).to(torch.float8_e4m3fn).view(torch.uint8).ravel(),
+                    torch.from_numpy(A16).to(torch.bfloat16).view(torch.uint8).ravel()])
+    tb = torch.cat([torch.from_numpy(B8).to(torch.float8_e4m3fn).view(torch.uint8).ravel(),
+                    torch.from_numpy(B16).to(torch.bfloat16).view(torch.uint8).ravel()])
+    got = _run_mma(V, 6, ta, tb)
+    ref = A8.astype(np.float64) @ B8.T + A16.astype(np.float64) @ B16.T
+    assert np.array_equal(got, ref)

@@ -1,0 +1,108 @@
+"""GPU: V-Smooth preparation (k-means labels, permutation, centroids, every
+quantised code, scale and mean) is bit-exact with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_prepare(q, k, v, kc, iters, seed, bits=8, reuse=False, state=None):
+    from bit_attention_video_gb300 import vca
+    B, H, N, d = q.shape
+    if state is None:
+        state = vca.alloc_state(B, H, N, d, kc, bits)
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, state, reuse, bits, iters, seed)
+    st = vca.get_status(state)
+    views = vca.state_view(state, (B, H, N, d), kc, bits)
+    return state, st, {n: t.cpu().numpy() for n, t in views.items()}
+
+
+def check_head8(g, p, bh, N, what=("labels", "perm", "centroids")):
+    for key in what:
+        assert np.array_equal(g[key][bh], p[key]), f"head {bh}: {key} differs"
+    pairs = [("qhat", "qhat"), ("sq", "sq"), ("khat", "khat"), ("sk", "sk"), ("rhatT", "rhatT"),
+             ("sv", "sv"), ("mutilde", "mutilde")]
+    for gk, pk in pairs:
+        a, b = g[gk][bh], p[pk]
+        if not np.array_equal(a, b):
+            bad = np.argwhere(a != b)
+            pytest.fail(f"head {bh}: {gk} differs at {len(bad)} places, first {bad[:3].tolist()}: "
+                        f"{a[tuple(bad[0])]} vs {b[tuple(bad[0])]}")
+    assert np.array_equal(g["kbar"][bh].view(np.uint16), p["kbar"]), f"head {bh}: kbar"
+    assert np.array_equal(g["mu"][bh].view(np.uint16), p["mu"]), f"head {bh}: mu"
+    # mean operand of the restoration MMA: (hi, hi, lo) of mutilde per channel
+    mt = torch.from_numpy(p["mutilde"])
+    hi = mt.to(torch.bfloat16)
+    lo = (mt - hi.float()).to(torch.bfloat16)
+    tile = g["mside"][bh].view(np.uint16).reshape(-1, 2048)
+    c = np.arange(128)
+    base = (c // 8) * 128 + (c % 8) * 8          # in bf16 elements
+    assert np.array_equal(tile[:, base], hi.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(tile[:, base + 1], hi.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(tile[:, base + 2], lo.view(torch.int16).numpy().view(np.uint16))
+    assert np.all(tile[:, base + 3] == 0) and np.all(tile[:, base[:, None] + 64 + np.arange(8)] == 0)
+
+
+@pytest.mark.parametrize("B,H,N,C,kc,iters", [
+    (1, 1, 1024, 16, 16, 10),    # the small parity configuration
+    (1, 2, 1000, 16, 16, 4),     # ragged last block
+    (2, 1, 300, 4, 8, 3),        # B > 1, three blocks
+    (1, 1, 128, 4, 4, 2),        # exactly one block
+    (1, 3, 1, 1, 1, 1),          # one token
+    (1, 1, 2500, 64, 200, 2),    # k > 96 (single accumulator group), several sort chunks
+])
+def test_prepare8_bit_exact(orc, B, H, N, C, kc, iters):
+    seed = 0xC0FFEE + N
+    q, k, v = synth.make_qkv(B, H, N, 128, C, seed)
+    _, st, g = gpu_prepare(q, k, v, kc, iters, seed)
+    assert st == 0
+    for b in range(B):
+        for h in range(H):
+            p = orc.prepare8(q[b, h], k[b, h], v[b, h], kc, iters, seed, b=b, h=h, H=H)
+            check_head8(g, p, b * H + h, N)
+
+
+def test_prepare8_h8_sampled_heads(orc):
+    w = synth.CONFIGS["h8"]
+    q, k, v = synth.make(w)
+    _, st, g = gpu_prepare(q, k, v, w.k, 10, w.seed)
+    assert st == 0
+    for h in (0, 5):
+        p = orc.prepare8(q[0, h], k[0, h], v[0, h], w.k, 10, w.seed, b=0, h=h, H=w.H)
+        check_head8(g, p, h, w.N)
+
+
+def test_reuse_permutation(orc):
+    B, H, N, kc = 1, 2, 900, 8
+    q, k, v = synth.make_qkv(B, H, N, 128, 8, 5)
+    q2, k2, v2 = synth.make_qkv(B, H, N, 128, 8, 6)      # the next "denoising step"
+    state, st, g1 = gpu_prepare(q, k, v, kc, 3, 9)
+    assert st == 0
+    state, st, g2 = gpu_prepare(q2, k2, v2, kc, 3, 9, reuse=True, state=state)
+    assert st == 0
+    assert np.array_equal(g1["perm"], g2["perm"])
+    for h in range(H):
+        p = orc.prepare8(q2[0, h], k2[0, h], v2[0, h], kc, 3, 9, perm=g1["perm"][h])
+        check_head8(g2, p, h, N, what=("perm",))
+
+
+def test_reuse_without_cached_permutation_is_reported(orc):
+    from bit_attention_video_gb300 import vca
+    B, H, N, kc = 1, 1, 300, 4
+    q, k, v = synth.make_qkv(B, H, N, 128, 4, 5)
+    state = vca.alloc_state(B, H, N, 128, kc, 8)
+    state.zero_()
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, state, True, 8, 2, 0)
+    assert vca.get_status(state) == -5
+    # a blob prepared with another k is refused as well
+    state2 = vca.alloc_state(B, H, N, 128, 8, 8)
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), 8, state2, False, 8, 2, 0)
+    assert vca.get_status(state2) == 0
+    big = torch.zeros(max(state.numel(), state2.numel()), dtype=torch.uint8, device="cuda")
+    big[:state2.numel()].copy_(state2)
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), 4, big, True, 8, 2, 0)
+    assert vca.get_status(big) == -5
