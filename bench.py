@@ -1,0 +1,343 @@
+#!/usr/bin/env python3
+"""VC-Attention benchmark on GB300.
+
+One step = the whole hot path on one batch of synthetic input resident in HBM:
+V-Smooth preparation (fresh k-means, permutation, Q/K/V quantisers) followed
+by the fused 8-bit attention.  The default workload is the Wan2.2-like 720p
+video-DiT shape B=1, H=40, N=75600 (21x45x80 tokens), d=128, k=64, 10 Lloyd
+iterations.  FLOPs are counted as 4 B H N^2 d (the two attention products).
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own full
+workload (independent problems, no collective on the data path): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan720p]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention TFLOPS & % of GB300 FP8 tensor peak at N=75600,H=40,d=128; V-Smooth ms"
+FP8_NOMINAL_TFLOPS = 4500.0   # dense FP8 per GPU (NVIDIA nominal)
+FP8_PER_BF16 = 2.0            # nominal FP8 : BF16 dense ratio
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sus=float(m["bf16_tflops_sustained"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def launches_per_step(iters: int, reuse: bool) -> int:
+    """Kernels of libvca launched by one step (preparation chain + attention)."""
+    grouping = 0 if reuse else (1 + 1 + 1 + 1 + 2 * iters + 3)  # zero, amax, features, init, iters, sort
+    return 1 + grouping + 7 + 1 + 1   # header, grouping, Q/K/V passes, header-done, attention
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([s.strip() for s in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 4 + i and r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_sample(w, rows_per_head=16, seed_rows=0):
+    """Time the CPU oracle on one head of the workload (full preparation and
+    `rows_per_head` attention rows), extrapolated to the whole workload."""
+    import oracle
+    oracle.build()
+    q, k, v = synth.make_qkv(1, 1, w.N, w.d, w.clusters, w.seed)
+    t0 = time.perf_counter()
+    p = oracle.prepare8(q[0, 0], k[0, 0], v[0, 0], w.k, 10, 0, b=0, h=0, H=1)
+    t_prep = time.perf_counter() - t0
+    rows = np.random.default_rng(seed_rows).choice(w.N, rows_per_head, replace=False)
+    t0 = time.perf_counter()
+    oracle.attention8(p, rows)
+    t_rows = time.perf_counter() - t0
+    heads = w.B * w.H
+    t_step = heads * (t_prep + t_rows * w.N / rows_per_head)
+    return dict(value=w.flops / t_step / 1e12, t_step_s=t_step, t_prep_head_s=t_prep,
+                t_rows_s=t_rows, sample=f"1 of {heads} heads: full V-Smooth preparation + "
+                f"{rows_per_head} of {w.N} attention rows, extrapolated linearly per head and row")
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times, vals = [], []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(w, rows_per_head=8, seed_rows=i)
+        if i >= args.warmup:
+            vals.append(r["value"])
+            times.append(r["t_step_s"])
+        sample = r["sample"]
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(times) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
+                       "bits": w.bits},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def time_e2e(e2e_step, args, stream, dist, dev):
+    import torch
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return ms
+
+
+def run_gpu(args, w):
+    import torch
+    from bit_attention_video_gb300 import vca
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    vca.lib()
+
+    shape = (w.B, w.H, w.N, w.d)
+    nbytes = w.B * w.H * w.N * w.d * 2
+    # inputs: generated once in pinned host memory (seed offset per rank)
+    host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    synth.make_qkv(w.B, w.H, w.N, w.d, w.clusters, w.seed + rank,
+                   out=tuple(h.view(torch.int16).numpy().view(np.uint16) for h in host))
+    q, k, v = (h.to(dev) for h in host)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    out_host = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    att = vca.VCAttention(*shape, k_clusters=w.k, bits=w.bits, iters=args.iters, seed=0,
+                          device=dev)
+    attn_fn = vca.attention_fp8 if w.bits == 8 else vca.attention_nvfp4
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        att.prepare(q, k, v, reuse_perm=args.reuse and att_ready[0])
+        if ev:
+            ev[1].record(stream)
+        attn_fn(att.state, shape, out)
+        if ev:
+            ev[2].record(stream)
+
+    att_ready = [False]
+    step()
+    att_ready[0] = True
+    st = att.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the first step")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    st = att.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    attn_avg = statistics.mean(attn_ms)
+    attn_tflops = w.flops / (attn_avg * 1e-3) / 1e12
+    pk = peaks()
+    fp8_peak = pk["bf16_sus"] * FP8_PER_BF16
+
+    # end to end through the public API: pinned H2D of Q, K, V, prepare,
+    # attention, D2H of O, every step
+    def e2e_step():
+        for h, d in zip(host, (q, k, v)):
+            d.copy_(h, non_blocking=True)
+        att.prepare(q, k, v)
+        attn_fn(att.state, shape, out)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_ms = None
+    if not args.no_e2e:
+        e2e_ms = time_e2e(e2e_step, args, stream, dist, dev)
+
+    # in-repo BF16
+ tcgen05 attention on the same inputs (the speedup denominator)
+    bf16_ms = None
+    if not args.skip_bf16:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            vca.attention_bf16_ref(q, k, v, out, status)
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        nb = max(1, min(args.steps, 5))
+        for _ in range(nb):
+            vca.attention_bf16_ref(q, k, v, out, status)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bf16_ms = b0.elapsed_time(b1) / nb
+        if vca.get_status(None, status) != 0:
+            bf16_ms = None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.bits == 8 else "e2m1", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
+                   "iters": args.iters, "bits": w.bits, "reuse_perm": bool(args.reuse),
+                   "step": "V-Smooth preparation + fused attention",
+                   "l2": "inputs (3 x %.2f GB) larger than L2; no flush" % (nbytes / 1e9),
+                   "parallelism": f"independent problem per GPU x{world}"},
+        "attention_ms": attn_avg, "attention_tflops": attn_tflops,
+        "pct_fp8_peak": 100.0 * attn_tflops / fp8_peak,
+        "pct_fp8_nominal": 100.0 * attn_tflops / FP8_NOMINAL_TFLOPS,
+        "vsmooth_ms": statistics.mean(prep_ms),
+        "vsmooth_gbs": None,
+        "bf16_ref_ms": bf16_ms,
+        "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": attn_tflops / fp8_peak, "traffic": None,
+                     "kernel": "attn_fp8_kernel",
+                     "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x {FP8_PER_BF16} "
+                                 "(nominal FP8:BF16 ratio)"},
+        "e2e": ({"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * nbytes,
+                 "d2h_bytes_per_step": nbytes} if e2e_ms else None),
+        "gpu_launches": launches_per_step(args.iters, args.reuse) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if dist:
+        dist.barrier()
+    if rank == 0 and not args.no_cpu_baseline:
+        r = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": r["value"], "unit": "TFLOPS", "cores": 1,
+                                "kind": "oracle", "sample": r["sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wan720p", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--iters", type=int, default=10)
+    ap.add_argument("--reuse", action="store_true", help="reuse the cached permutation")
+    ap.add_argument("--skip-bf16", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

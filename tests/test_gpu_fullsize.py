@@ -1,0 +1,40 @@
+"""GPU: the full Wan2.2-like 720p workload (B=1, H=40, N=75600, k=64, 10
+iterations) in the launch configuration the benchmark times; preparation of
+two sampled heads is bit-exact with the oracle and sampled attention rows are
+within relative L2 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import bf16_f64, rel_l2, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wan720p_sampled_parity(orc):
+    from bit_attention_video_gb300 import vca
+    w = synth.CONFIGS["wan720p"]
+    shape = (w.B, w.H, w.N, w.d)
+    host = [torch.empty(shape, dtype=torch.bfloat16) for _ in range(3)]
+    q, k, v = synth.make_qkv(w.B, w.H, w.N, w.d, w.clusters, w.seed,
+                             out=tuple(h.view(torch.int16).numpy().view(np.uint16) for h in host))
+    dq, dk, dv = (h.cuda() for h in host)
+    att = vca.VCAttention(*shape, k_clusters=w.k, bits=8, iters=10, seed=0)
+    out = att(dq, dk, dv)
+    assert att.status() == 0
+    views = vca.state_view(att.state, shape, w.k, 8)
+    rng = np.random.default_rng(20)
+    for h in (0, w.H - 1):
+        p = orc.prepare8(q[0, h], k[0, h], v[0, h], w.k, 10, 0, b=0, h=h, H=w.H)
+        for key in ("labels", "perm", "qhat", "sq", "khat", "sk", "rhatT", "sv", "mutilde"):
+            g = views[key][h].cpu().numpy()
+            assert np.array_equal(g, p[key]), f"head {h}: {key}"
+        assert np.array_equal(views["mu"][h].cpu().numpy().view(np.uint16), p["mu"])
+        rows = np.sort(np.concatenate([rng.choice(w.N - 128, 24, replace=False),
+                                       np.arange(w.N - 8, w.N)]))   # include the ragged tail
+        _, ref = orc.attention8(p, rows)
+        got = bf16_f64(to_np_u16(out[0, h][torch.from_numpy(rows).cuda()]))
+        err = rel_l2(got, ref)
+        print(f"head {h}: relative L2 vs oracle {err:.2e}")
+        assert err <= 2e-3
