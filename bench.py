@@ -260,8 +260,7 @@ def run_gpu(args, w):
     if not args.no_e2e:
         e2e_ms = time_e2e(e2e_step, args, stream, dist, dev)
 
-    # in-repo BF16
- tcgen05 attention on the same inputs (the speedup denominator)
+    # in-repo BF16 tcgen05 attention on the same inputs (the speedup denominator)
     bf16_ms = None
     if not args.skip_bf16:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
