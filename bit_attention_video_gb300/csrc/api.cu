@@ -43,7 +43,7 @@ int compute_layout(int B, int H, int N, int d, int k, int bits, vca_state_layout
     L->r4s = take(BH * d * Npad / 16);
     L->g4 = take(BH * 16);
   }
-  L->mside = take(BH * nb * kSideTileBytes);
+  L->mside = take(BH * ((nb + kGroup - 1) / kGroup) * kGroupBytes);
   L->mu = take(BH * nb * d * 2);
   L->kbar = take(BH * d * 2);
   L->perm = take(BH * N * 4);

@@ -484,30 +484,34 @@ __global__ void __launch_bounds__(128) vpass1_kernel(const uint16_t* v, const in
   vamax[((size_t)bh * nb + j) * 128 + c] = amax;
 }
 
-// grid BH, 128 threads: sv = max over blocks / 448; mutilde = mu / sv; the
-// mean operand of the restoration MMA: per block a 128 (channel) x 16 bf16
-// K-major tile without swizzle whose K columns 0, 1, 2 hold (hi, hi, lo) of
-// mutilde (the A side supplies (r_hi, r_lo, r_hi)).
+// grid BH, 128 threads: sv = max over blocks / 448; mutilde = mu / sv; and
+// the mean operand of the restoration MMA (zeroed beforehand).  Blocks form
+// groups of kGroup, aligned to the last block (block j is slot (j + gpad) %
+// kGroup of group (j + gpad) / kGroup); per group two 128 (channel) x 16 (K)
+// bf16 K-major chunks without swizzle, element (c, k) at (c/8)*256 +
+// (k/8)*128 + (c%8)*16 + (k%8)*2: chunk 0 holds bf16(mutilde), chunk 1 the
+// bf16 of the remainder; K columns kGroup..15 and leading empty slots stay 0.
 __global__ void vreduce_kernel(const float* vamax, const uint16_t* mu, float* sv, float* mutilde,
-                               uint8_t* mside, int nb, const int* status) {
+                               uint8_t* mside, int nb, int ngroups, int gpad, const int* status) {
   if (prep_skip(status)) return;
   const int bh = blockIdx.x, c = threadIdx.x;
   float m = 0.0f;
   for (int j = 0; j < nb; ++j) m = fmaxf(m, vamax[((size_t)bh * nb + j) * 128 + c]);
   const float s = e4m3_scale(m);
   sv[(size_t)bh * 128 + c] = s;
+  uint8_t* gbase = mside + (size_t)bh * ngroups * kGroupBytes;
+  const uint32_t coff = (c / 8) * 256 + (c % 8) * 16;
   for (int j = 0; j < nb; ++j) {
     const size_t o = ((size_t)bh * nb + j) * 128 + c;
     const float mt = __fdiv_rn(bf16_bits_to_f32(mu[o]), s);
     mutilde[o] = mt;
     const uint16_t hi = f32_to_bf16_bits(mt);
     const uint16_t lo = f32_to_bf16_bits(__fsub_rn(mt, bf16_bits_to_f32(hi)));
-    uint8_t* tile = mside + ((size_t)bh * nb + j) * kSideTileBytes;
-    // element (n = c, k) at (c/8)*256 + (k/8)*128 + (c%8)*16 + (k%8)*2
-    uint4* p0 = reinterpret_cast<uint4*>(tile + (c / 8) * 256 + (c % 8) * 16);
-    uint4* p1 = reinterpret_cast<uint4*>(tile + (c / 8) * 256 + 128 + (c % 8) * 16);
-    *p0 = make_uint4((uint32_t)hi | ((uint32_t)hi << 16), (uint32_t)lo, 0u, 0u);
-    *p1 = make_uint4(0u, 0u, 0u, 0u);
+    const int g = (j + gpad) / kGroup, k = (j + gpad) % kGroup;
+    uint8_t* tile = gbase + (size_t)g * kGroupBytes;
+    const uint32_t off = coff + (k / 8) * 128 + (k % 8) * 2;
+    *reinterpret_cast<uint16_t*>(tile + off) = hi;
+    *reinterpret_cast<uint16_t*>(tile + kGroupBytes / 2 + off) = lo;
   }
 }
 
@@ -611,7 +615,11 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
   quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
   vpass1_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, vamax, N, nb, status);
-  vreduce_kernel<<<BH, 128, 0, st>>>(vamax, mu, sv, mut, mside, nb, status);
+  const int ngroups = (nb + kGroup - 1) / kGroup;
+  zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroupBytes / 4, 256, 4096), 256, 0, st>>>(
+      reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroupBytes / 4);
+  vreduce_kernel<<<BH, 128, 0, st>>>(vamax, mu, sv, mut, mside, nb, ngroups,
+                                     ngroups * kGroup - nb, status);
   vpass2_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, sv, rhatT, N, Npad, nb, status);
   header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;

@@ -9,8 +9,12 @@
 namespace vca {
 
 constexpr uint32_t kStateMagic = 0x31414356u;  // "VCA1"
-constexpr uint32_t kSideTileBytes = 128 * 16 * 2;  // bf16 128 x 16 mean operand per block
 constexpr uint32_t kTileBytes = 128 * 128;         // one 128 x 128 E4M3 tile
+// Mean operand of the restoration MMA for a group of kGroup key blocks: two
+// 128 (channel) x 16 (K) bf16 K-major chunks without swizzle (hi, lo); slot k
+// of the group is K column k, columns kGroup..15 are zero.
+constexpr int kGroup = 8;
+constexpr uint32_t kGroupBytes = 2 * 128 * 16 * 2;
 
 // Header words (uint32): magic, B, H, N, d, k, bits, perm cached, operands ready.
 

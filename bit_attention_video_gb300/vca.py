@@ -180,7 +180,8 @@ def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
         centroids=v(L.centroids, BH * k_clusters * d, torch.int8, (BH, k_clusters, d)),
         kbar=v(L.kbar, BH * d, torch.int16, (BH, d)),
         mu=v(L.mu, BH * nb * d, torch.int16, (BH, nb, d)),
-        mside=v(L.mside, BH * nb * 2048, torch.int16, (BH, nb, 2048)),
+        mside=v(L.mside, BH * ((nb + 7) // 8) * 4096, torch.int16,
+                (BH, (nb + 7) // 8, 2, 2048)),
         status=v(L.status, 1, torch.int32, (1,)),
     )
     if bits == 8:

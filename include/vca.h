@@ -75,7 +75,7 @@ typedef struct {
   uint64_t sv;        /* fp32  [BH][d]     per-channel residual scales */
   uint64_t mu;        /* bf16  [BH][nb][d] block means (unscaled) */
   uint64_t mutilde;   /* fp32  [BH][nb][d] mu / sv */
-  uint64_t mside;     /* bf16  [BH][nb][128*16] mean operand of the restoration MMA */
+  uint64_t mside;     /* bf16  [BH][ceil(nb/8)][2][128*16] mean operand of the restoration MMA */
   uint64_t vamax;     /* fp32  [BH][nb][d] per-block residual channel maxima (scratch) */
   /* 4-bit (NVFP4) path */
   uint64_t q4;        /* e2m1 packed [BH][Npad][d/2] */

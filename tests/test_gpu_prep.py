@@ -34,17 +34,28 @@ def check_head8(g, p, bh, N, what=("labels", "perm", "centroids")):
                         f"{a[tuple(bad[0])]} vs {b[tuple(bad[0])]}")
     assert np.array_equal(g["kbar"][bh].view(np.uint16), p["kbar"]), f"head {bh}: kbar"
     assert np.array_equal(g["mu"][bh].view(np.uint16), p["mu"]), f"head {bh}: mu"
-    # mean operand of the restoration MMA: (hi, hi, lo) of mutilde per channel
+    # mean operand of the restoration MMA: per group of 8 blocks (aligned to
+    # the last block) chunk 0 = bf16(mutilde), chunk 1 = bf16 remainder, K
+    # columns 8..15 zero
     mt = torch.from_numpy(p["mutilde"])
     hi = mt.to(torch.bfloat16)
     lo = (mt - hi.float()).to(torch.bfloat16)
-    tile = g["mside"][bh].view(np.uint16).reshape(-1, 2048)
+    hi = hi.view(torch.int16).numpy().view(np.uint16)
+    lo = lo.view(torch.int16).numpy().view(np.uint16)
+    nb = p["mutilde"].shape[0]
+    ng = (nb + 7) // 8
+    gpad = ng * 8 - nb
+    tiles = g["mside"][bh].view(np.uint16).reshape(ng, 2, 2048)
     c = np.arange(128)
-    base = (c // 8) * 128 + (c % 8) * 8          # in bf16 elements
-    assert np.array_equal(tile[:, base], hi.view(torch.int16).numpy().view(np.uint16))
-    assert np.array_equal(tile[:, base + 1], hi.view(torch.int16).numpy().view(np.uint16))
-    assert np.array_equal(tile[:, base + 2], lo.view(torch.int16).numpy().view(np.uint16))
-    assert np.all(tile[:, base + 3] == 0) and np.all(tile[:, base[:, None] + 64 + np.arange(8)] == 0)
+    for slot_j in range(-gpad, nb):
+        gi, k = divmod(slot_j + gpad, 8)
+        idx = (c // 8) * 128 + (k // 8) * 64 + (c % 8) * 8 + (k % 8)   # in bf16 elements
+        want_hi = hi[slot_j] if slot_j >= 0 else 0
+        want_lo = lo[slot_j] if slot_j >= 0 else 0
+        assert np.array_equal(tiles[gi, 0, idx], np.broadcast_to(want_hi, (128,))), slot_j
+        assert np.array_equal(tiles[gi, 1, idx], np.broadcast_to(want_lo, (128,))), slot_j
+    upper = (c[:, None] // 8) * 128 + 64 + (c[:, None] % 8) * 8 + np.arange(8)[None, :]
+    assert np.all(tiles[:, :, upper.ravel()] == 0)
 
 
 @pytest.mark.parametrize("B,H,N,C,kc,iters", [
