@@ -7,7 +7,8 @@
 //   warp 0        producer: TMA of the Q tile once; per stage K'_j, R^T_j and
 //                 the 16 "slot" rows appended to R^T_j (written by the warp's
 //                 lanes); the mean operand of each group of 8 blocks
-//   warp 1        MMA issuer (one thread, busy-polling) and TMEM owner
+//   warp 1        MMA issuer (warp-uniform loop, one elected lane issues;
+//                 busy-polling) and TMEM owner
 //   warps 4-11    softmax + correction + epilogue: two threads per query row
 //                 (key columns 0-63 and 64-127, output columns 0-63 and
 //                 64-127), which exchange the partial row maximum
@@ -212,64 +213,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop (uniform control flow, operands in
+    // uniform registers); one elected lane issues each MMA and commit.
     // S_0, S_1 up front; per block j, once P^_j is in TMEM: P^ [R^_j; E_j],
     // the mean product of a group closed by block j-1, and S_{j+2} into the
     // buffer the softmax released after reading S_j.
-    if (lane == 0) {
+    {
       const uint32_t i8 = idesc_f8(128, 128), i8w = idesc_f8(128, 144),
                      i16 = idesc_bf16(128, 128);
       const uint64_t dq = desc_k_sw128(base + OFF_Q);
       const uint64_t dk0 = desc_k_sw128(base + OFF_KV);                  // stage 0 K'
       const uint64_t dr0 = desc_k_sw128(base + OFF_KV + kTileBytes);     // stage 0 [R^; E]
       const uint64_t dstage = kStageBytes >> 4;                          // per-stage step
+      const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256);
+      const uint64_t dgroup = kGroupBytes >> 4, dhalf = (kGroupBytes / 2) >> 4;
       bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, p.status);
       auto issue_s = [&](int j) {
         const int s = j % kStages;
-        if (!(ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status)))
-          return;
+        ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
         tc_fence_after();
         const uint64_t dk = dk0 + s * dstage;
         const uint32_t d = tmem + TC_S + 128 * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_f8_ss(d, dq + 2 * kk, dk + 2 * kk, i8, kk > 0);
-        mma_commit(bar(B_SFULL + (j & 1)));
+        for (int kk = 0; kk < 4; ++kk) mma_f8_ss_w(d, dq + 2 * kk, dk + 2 * kk, i8, kk > 0);
+        mma_commit_w(bar(B_SFULL + (j & 1)));
       };
+      auto issue_flush = [&](int g) {
+        // sum_g rho_g mutilde_g^T = rho_hi mu_hi + rho_lo mu_hi + rho_hi mu_lo
+        const uint64_t bg = dbg0 + (g & 1) * dgroup;
+        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GHI, bg, i16, 1);
+        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GLO, bg, i16, 1);
+        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GHI, bg + dhalf, i16, 1);
+      };
+      ok = __all_sync(0xffffffffu, ok);
       for (int j = 0; ok && j < min(2, nb); ++j) issue_s(j);
       for (int j = 0; ok && j < nb; ++j) {
-        if (!(ok = mbar_wait_spin(bar(B_PFULL), j & 1, abort_flag, p.status))) break;
+        ok = mbar_wait_spin(bar(B_PFULL), j & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint64_t dr = dr0 + (j % kStages) * dstage;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f8_ts(tmem + TC_ACC, tmem + TC_P + 8 * kk, dr + 2 * kk, i8w, (j > 0 || kk > 0));
-        if (j > 0 && group_ends(j - 1, nb, gpad)) {
-          // sum_g rho_g mutilde_g^T = rho_hi mu_hi + rho_lo mu_hi + rho_hi mu_lo
-          const uint32_t bg = base + OFF_BG + ((((j - 1 + gpad) / kGroup) & 1) * kGroupBytes);
-          mma_f16_ts(tmem + TC_ACC, tmem + TC_GHI, desc_k_plain(bg, 128, 256), i16, 1);
-          mma_f16_ts(tmem + TC_ACC, tmem + TC_GLO, desc_k_plain(bg, 128, 256), i16, 1);
-          mma_f16_ts(tmem + TC_ACC, tmem + TC_GHI, desc_k_plain(bg + kGroupBytes / 2, 128, 256),
-                     i16, 1);
-        }
-        mma_commit(bar(B_PVDONE));
-        mma_commit(bar(B_KVEMPTY + j % kStages));
+          mma_f8_ts_w(tmem + TC_ACC, tmem + TC_P + 8 * kk, dr + 2 * kk, i8w, (j > 0 || kk > 0));
+        if (j > 0 && group_ends(j - 1, nb, gpad)) issue_flush((j - 1 + gpad) / kGroup);
+        mma_commit_w(bar(B_PVDONE));
+        mma_commit_w(bar(B_KVEMPTY + j % kStages));
         if (j + 2 < nb) {
-          if (!(ok = mbar_wait_spin(bar(B_SFREE + (j & 1)), (j >> 1) & 1, abort_flag, p.status)))
-            break;
+          ok = mbar_wait_spin(bar(B_SFREE + (j & 1)), (j >> 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           issue_s(j + 2);
         }
       }
       // the last group's mean product, after the softmax read its row sums
-      if (ok && (ok = mbar_wait_spin(bar(B_PFULL), nb & 1, abort_flag, p.status))) {
-        tc_fence_after();
-        const uint32_t bg = base + OFF_BG + ((((nb - 1 + gpad) / kGroup) & 1) * kGroupBytes);
-        mma_f16_ts(tmem + TC_ACC, tmem + TC_GHI, desc_k_plain(bg, 128, 256), i16, 1);
-        mma_f16_ts(tmem + TC_ACC, tmem + TC_GLO, desc_k_plain(bg, 128, 256), i16, 1);
-        mma_f16_ts(tmem + TC_ACC, tmem + TC_GHI, desc_k_plain(bg + kGroupBytes / 2, 128, 256),
-                   i16, 1);
-        mma_commit(bar(B_PVDONE));
+      if (ok) {
+        ok = mbar_wait_spin(bar(B_PFULL), nb & 1, abort_flag, p.status);
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after();
+          issue_flush((nb - 1 + gpad) / kGroup);
+          mma_commit_w(bar(B_PVDONE));
+        }
       }
       // all issued MMAs complete before the CTA releases its tensor memory
-      mma_commit(bar(B_DRAIN));
+      mma_commit_w(bar(B_DRAIN));
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }

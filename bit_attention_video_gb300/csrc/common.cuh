@@ -204,6 +204,40 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t 
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
 }
+// Warp-uniform forms: every lane of the warp executes the call with the same
+// operands (so the compiler keeps them in uniform registers) and the lowest
+// active lane, chosen by elect.sync, issues the instruction.
+__device__ __forceinline__ void mma_f8_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nelect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, q;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nelect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, q;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nelect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\n"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
