@@ -626,3 +626,93 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
 }
 
 }  // namespace vca
+
+// ---------------------------------------------------------------------------
+// Grouping without caller-provided scratch
+// ---------------------------------------------------------------------------
+namespace vca {
+namespace {
+
+// Scratch of vca_kmeans_permutation_noalloc: a fixed array in this library's
+// device image, present on every GPU that loads the library until the process
+// exits.  Layout (bytes): [0,256) status word, [256,512) |V| maximum and grid
+// scale, then the int8 features [kNoAllocMaxTokens x 128], the int8 centroids
+// [256 x 128], the int32 cluster sums [256 x 128] and counts [256], and the
+// sort histogram [256 x kNoAllocMaxTokens / kSortChunk].
+constexpr size_t kNaOffStatus = 0, kNaOffAmax = 256, kNaOffX = 512;
+constexpr size_t kNaOffCent = kNaOffX + (size_t)VCA_NOALLOC_MAX_TOKENS * 128;
+constexpr size_t kNaOffSums = kNaOffCent + 256 * 128;
+constexpr size_t kNaOffHist = kNaOffSums + (256 * 128 + 256) * 4;
+constexpr size_t kNaBytes = kNaOffHist + 256 * (VCA_NOALLOC_MAX_TOKENS / kSortChunk) * 4;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNaBytes];
+
+// Device address of the scratch array on each device (the host-side symbol is
+// only a stand-in, not a device address).  Filled by the first call on a device.
+constexpr int kMaxDevices = 64;
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace vca
+
+extern "C" int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters,
+                                              int iters, uint64_t seed, int b, int h, int H,
+                                              int32_t* labels, int32_t* perm,
+                                              vca_stream_t stream) {
+  using namespace vca;
+  if (!v || !labels || !perm) return VCA_ERR_INVALID_ARG;
+  if (((uintptr_t)v & 15u) || ((uintptr_t)labels & 3u) || ((uintptr_t)perm & 3u))
+    return VCA_ERR_INVALID_ARG;
+  if (d != 128 || N < 1 || N > VCA_NOALLOC_MAX_TOKENS) return VCA_ERR_UNSUPPORTED;
+  if (k_clusters < 1 || k_clusters > 256 || k_clusters > N) return VCA_ERR_UNSUPPORTED;
+  if (iters < 1 || iters > 1000 || b < 0 || h < 0 || H < 1 || h >= H) return VCA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VCA_ERR_CUDA;
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return VCA_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  uint8_t* S = g_noalloc_ptr[dev];
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int k = k_clusters;
+  const size_t per_head = (size_t)N * 128;
+  int* status = reinterpret_cast<int*>(S + kNaOffStatus);
+  uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + kNaOffAmax);
+  float* gscale = reinterpret_cast<float*>(S + kNaOffAmax + 4);
+  int8_t* x = reinterpret_cast<int8_t*>(S + kNaOffX);
+  int8_t* cent = reinterpret_cast<int8_t*>(S + kNaOffCent);
+  int32_t* sums = reinterpret_cast<int32_t*>(S + kNaOffSums);
+  int32_t* counts = sums + (size_t)k * 128;
+  int32_t* hist = reinterpret_cast<int32_t*>(S + kNaOffHist);
+  const uint16_t* vv = static_cast<const uint16_t*>(v);
+  // The initial centroids of head (b, h) come from SplitMix64 seeded with
+  // seed ^ (0x9E3779B97F4A7C15 * (b*H + h + 1)); the init kernel mixes in its
+  // block index (0 here) the same way, so the seed is pre-mixed to match.
+  const uint64_t G = 0x9E3779B97F4A7C15ull;
+  const uint64_t seed_mixed = seed ^ (G * (uint64_t)((int64_t)b * H + h + 1)) ^ G;
+
+  // the leftover contents of the previous call are cleared where needed:
+  // status and maximum here, centroid sums and counts by the init kernel
+  zero_kernel<<<1, 32, 0, st>>>(reinterpret_cast<uint32_t*>(S), 2 * 256 / 4);
+  const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
+  head_amax_kernel<<<dim3(ch, 1), 256, 0, st>>>(vv, amax_bits, per_head, status);
+  features_kernel<<<dim3(ch, 1), 256, 0, st>>>(vv, amax_bits, gscale, x, per_head, status);
+  kmeans_init_kernel<<<1, 128, 0, st>>>(x, cent, sums, counts, seed_mixed, N, k, 128, status);
+  const int groups = k <= 96 ? 2 : 1;
+  const size_t asmem = assign_smem_bytes(k, groups);
+  if (cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)asmem) != cudaSuccess)
+    return VCA_ERR_CUDA;
+  const int tiles = (N + kAssignTokens - 1) / kAssignTokens;
+  for (int it = 0; it < iters; ++it) {
+    kmeans_assign_kernel<<<dim3(tiles, 1), 256, asmem, st>>>(x, cent, labels, sums, counts, N, k,
+                                                             groups, status);
+    kmeans_update_kernel<<<dim3(1, k), 128, 0, st>>>(cent, sums, counts, k, status);
+  }
+  const int nchunk = (N + kSortChunk - 1) / kSortChunk;
+  sort_hist_kernel<<<dim3(nchunk, 1), 256, 0, st>>>(labels, hist, N, k, nchunk, status);
+  sort_scan_kernel<<<1, 256, 0, st>>>(hist, k, nchunk, status);
+  sort_scatter_kernel<<<dim3(nchunk, 1), 256, 0, st>>>(labels, hist, perm, N, k, nchunk, status);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+

@@ -67,6 +67,8 @@ def lib():
         L.vca_debug_encode.argtypes = [P, P, P, S, P]
         L.vca_debug_mma.restype = I
         L.vca_debug_mma.argtypes = [I, P, P, P, P]
+        L.vca_kmeans_permutation_noalloc.restype = I
+        L.vca_kmeans_permutation_noalloc.argtypes = [P, I, I, I, I, U64, I, I, I, P, P, P]
         _lib = L
     return _lib
 
@@ -143,6 +145,18 @@ def get_status(state=None, status_word=None, stream=None) -> int:
     return lib().vca_get_status(_dev(state) if state is not None else None,
                                 _dev(status_word) if status_word is not None else None,
                                 _stream(stream))
+
+
+NOALLOC_MAX_TOKENS = 32768
+
+
+def kmeans_permutation_noalloc(v_head, k_clusters, labels, perm, iters=DEFAULT_ITERS,
+                               seed=DEFAULT_SEED, b=0, h=0, H=1, stream=None):
+    """Grouping of one head without a state blob (scratch inside the library)."""
+    N, d = v_head.shape
+    _check("vca_kmeans_permutation_noalloc", lib().vca_kmeans_permutation_noalloc(
+        _dev(v_head, torch.bfloat16), N, d, k_clusters, iters, seed, b, h, H,
+        _dev(labels, torch.int32), _dev(perm, torch.int32), _stream(stream)))
 
 
 def debug_expcast(acc, a, b, out, stream=None):

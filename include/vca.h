@@ -146,6 +146,30 @@ int vca_get_status(void* state, int* status_word, vca_stream_t stream);
 /* Human-readable name of a vca_status value. */
 const char* vca_status_string(int status);
 
+/* Largest N accepted by vca_kmeans_permutation_noalloc. */
+#define VCA_NOALLOC_MAX_TOKENS 32768
+
+/* The grouping step (k-means labels and the stable permutation) for one
+ * (batch, head) of V, for callers that cannot allocate device memory: code
+ * whose device memory is handed out by a host framework's own pool, or loops
+ * that must not pay cudaMalloc's implicit synchronisation.  This entry point
+ * has no counterpart in the paper; it computes exactly what
+ * vca_vsmooth_prepare stores as `labels` and `perm` for head (b, h) of an
+ * H-head problem (same seed rule), without a state blob.
+ *   v       bf16 [N, 128] device pointer (16-byte aligned), one head
+ *   labels  int32 [N] device output, perm int32 [N] device output
+ *   N <= VCA_NOALLOC_MAX_TOKENS, else VCA_ERR_UNSUPPORTED (nothing launched).
+ * Its scratch (about 4.3 MB) is a fixed array inside this library's device
+ * image; every GPU that loads the library holds it until the process exits.
+ * It allocates and frees nothing.  The first call on a device looks up the
+ * array's device address once (cudaGetSymbolAddress), so make that first
+ * call before capturing any stream.  All calls share the one array: calls
+ * whose execution overlaps on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller. */
+int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters, int iters,
+                                   uint64_t seed, int b, int h, int H, int32_t* labels,
+                                   int32_t* perm, vca_stream_t stream);
+
 /* ---- test entry points (device buffers) ---- */
 
 /* ExpCast-FP8 device function on n inputs: out[i] = clip_[0,120](RNE(fma(a[i],
