@@ -49,7 +49,9 @@ def peaks():
 def launches_per_step(iters: int, reuse: bool) -> int:
     """Kernels of libvca launched by one step (preparation chain + attention)."""
     grouping = 0 if reuse else (1 + 1 + 1 + 1 + 2 * iters + 3)  # zero, amax, features, init, iters, sort
-    return 1 + grouping + 7 + 1 + 1   # header, grouping, Q/K/V passes, header-done, attention
+    # header, grouping, Q/K/V passes (Q, K sums, K mean, K, V1, V reduce, zero, V2),
+    # header-done, attention
+    return 1 + grouping + 8 + 1 + 1
 
 
 class ClockSampler:

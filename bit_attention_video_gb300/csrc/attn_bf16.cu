@@ -123,49 +123,55 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // Warp-uniform loop; one elected lane issues each MMA and commit.
+    {
       const uint32_t iqk = idesc_bf16(128, 128), ipv = idesc_bf16(128, 128, true);
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, status);
+      const uint64_t dq0 = desc_k_sw128(base + OFF_Q), dk0 = desc_k_sw128(base + OFF_KV);
+      const uint64_t dv0 = make_desc(base + OFF_KV + kTile, kHalf, 1024, 2);
+      const uint64_t dstage = kStageBytes >> 4, dtile = kTile >> 4, dhalf = kHalf >> 4;
+      bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, status);
       // Per tile: PV_j^t as soon as its probabilities are in TMEM, then S_{j+1}^t
       // once PV_j^t has consumed them (P aliases the S columns).  The tiles
       // alternate, so one tile's products overlap the other's softmax.
       auto issue_s = [&](int j, int t) {
-        const uint32_t st = base + OFF_KV + (j % kStages) * kStageBytes;
-        const uint32_t qa = base + OFF_Q + t * kTile;
+        const uint64_t dk = dk0 + (j % kStages) * dstage, dq = dq0 + t * dtile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t o = (kk / 4) * kHalf + (kk % 4) * 32;
-          mma_f16_ss(tmem + 256 * t, desc_k_sw128(qa + o), desc_k_sw128(st + o), iqk, kk > 0);
+          const uint64_t o = (kk / 4) * dhalf + (kk % 4) * 2;
+          mma_f16_ss_w(tmem + 256 * t, dq + o, dk + o, iqk, kk > 0);
         }
-        mma_commit(bar(B_SFULL + t));
+        mma_commit_w(bar(B_SFULL + t));
       };
-      if (ok) ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, status);
-      if (ok) {
+      if (ok) ok = mbar_wait_spin(bar(B_KVFULL), 0, abort_flag, status);
+      if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         for (int t = 0; t < ntiles; ++t) issue_s(0, t);
+      } else {
+        ok = false;
       }
       for (int j = 0; ok && j < p.nb; ++j) {
-        const uint32_t st = base + OFF_KV + (j % kStages) * kStageBytes;
+        const uint64_t dv = dv0 + (j % kStages) * dstage;
         for (int t = 0; t < ntiles && ok; ++t) {
-          if (!(ok = mbar_wait(bar(B_PFULL + t), j & 1, abort_flag, status))) break;
+          ok = mbar_wait_spin(bar(B_PFULL + t), j & 1, abort_flag, status);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk,
-                       make_desc(st + kTile + kk * 2048, kHalf, 1024, 2), ipv, (j > 0 || kk > 0));
-          mma_commit(bar(B_PVDONE + t));
+            mma_f16_ts_w(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk, dv + kk * (2048 >> 4), ipv,
+                         (j > 0 || kk > 0));
+          mma_commit_w(bar(B_PVDONE + t));
           if (j + 1 < p.nb) {
             const int s1 = (j + 1) % kStages;
-            if (t == 0 && !(ok = mbar_wait(bar(B_KVFULL + s1), ((j + 1) / kStages) & 1, abort_flag, status)))
-              break;
-            if (!(ok = mbar_wait(bar(B_PVDONE + t), j & 1, abort_flag, status))) break;
+            if (t == 0) ok = mbar_wait_spin(bar(B_KVFULL + s1), ((j + 1) / kStages) & 1, abort_flag, status);
+            if (ok) ok = mbar_wait_spin(bar(B_PVDONE + t), j & 1, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             issue_s(j + 1, t);
           }
         }
-        if (ok) mma_commit(bar(B_KVEMPTY + j % kStages));
+        if (ok) mma_commit_w(bar(B_KVEMPTY + j % kStages));
       }
-      mma_commit(bar(B_DRAIN));
+      mma_commit_w(bar(B_DRAIN));
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }

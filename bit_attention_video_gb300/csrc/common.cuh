@@ -223,6 +223,14 @@ __device__ __forceinline__ void mma_f8_ts_w(uint32_t d, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
 }
+__device__ __forceinline__ void mma_f16_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nelect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
 __device__ __forceinline__ void mma_f16_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b,
                                              uint32_t idesc, uint32_t accum) {
   asm volatile(

@@ -235,6 +235,188 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
   }
 }
 
+// One Lloyd iteration on the tensor cores, for k <= 128.  grid
+// (ceil(N / (128*kTcTiles)), BH), 256 threads.  Per 128-token tile, with the int8 features and centroids
+// held as bf16 (exact for |x| <= 127) and fp32 accumulation (exact: every dot
+// product and every per-CTA sum stays below 2^24):
+//   D_a = X C^T       (M = 128 tokens, N = kpad centroids, K = 128 channels)
+//   label_t = argmin_m ||c_m||^2 - 2 D_a[t, m]  (lowest index on ties)
+//   D_u += H^T X      (M = 128 cluster rows, N = 128 channels, K = 128 tokens)
+// with H the one-hot label matrix.  The X tile is one shared-memory image:
+// K-major (128-byte swizzle) as the A operand of the first product and
+// MN-major as the B operand of the second.  The CTA's cluster sums D_u and
+// counts are added to the global sums once at the end.
+constexpr int kTcTiles = 8;
+constexpr uint32_t kTcX = 0, kTcH = 32768, kTcC = 65536;  // smem: X, H^T, C (kpad x 256 B)
+inline size_t kmeans_tc_smem_bytes(int kpad) { return kTcC + (size_t)kpad * 256 + 1024 + 2048; }
+
+__global__ void __launch_bounds__(256) kmeans_assign_tc_kernel(const int8_t* x, const int8_t* cent,
+                                                               int32_t* labels, int32_t* sums,
+                                                               int32_t* counts, int N, int k,
+                                                               int kpad, const int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  __shared__ int32_t cnt[256];
+  __shared__ int32_t cnorm[256];
+  if (prep_skip(status)) return;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int bh = blockIdx.y, tile0 = blockIdx.x * kTcTiles;
+  const int ntile_head = (N + 127) / 128;
+  const int ntiles = min(kTcTiles, ntile_head - tile0);
+  const uint32_t ncols = kpad <= 128 ? 256 : 512, col_u = kpad <= 128 ? 128 : 256;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+  }
+  // centroids -> bf16, K-major 128-byte swizzle: two atoms of kpad rows x 64
+  // channels; rows k..kpad-1 are zero
+  const int8_t* cg = cent + (size_t)bh * k * 128;
+  for (int i = tid; i < kpad * 16; i += 256) {  // one 16-byte chunk (8 channels) per step
+    const int m = i / 16, c8 = i % 16, atom = c8 / 8, ch = c8 % 8;
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (m < k) {
+      const uint2 src = *reinterpret_cast<const uint2*>(cg + (size_t)m * 128 + c8 * 8);
+      const uint32_t sv[2] = {src.x, src.y};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float f = (float)(int8_t)((sv[e / 4] >> (8 * (e % 4))) & 0xFF);
+        const uint32_t bits = f32_to_bf16_bits(f);
+        w[e / 2] |= bits << (16 * (e % 2));
+      }
+    }
+    *reinterpret_cast<uint4*>(sm + kTcC + atom * kpad * 128 + m * 128 + ((ch ^ (m & 7)) << 4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  for (int m = tid; m < 256; m += 256) {
+    cnt[m] = 0;
+    int32_t n2 = 0;
+    if (m < k)
+      for (int c = 0; c < 128; ++c) {
+        const int v = cg[(size_t)m * 128 + c];
+        n2 += v * v;
+      }
+    cnorm[m] = n2;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t ia = idesc_bf16(128, kpad), iu = idesc_bf16(128, 128, true);
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int tt = 0; tt < ntiles && ok; ++tt) {
+    const int t0 = (tile0 + tt) * 128;
+    // X tile: token rows, bf16, K-major swizzled; H^T tile cleared
+    const int8_t* xg = x + ((size_t)bh * N + t0) * 128;
+    for (int i = tid; i < 128 * 16; i += 256) {
+      const int t = i / 16, c8 = i % 16, atom = c8 / 8, ch = c8 % 8;
+      uint32_t w[4] = {0, 0, 0, 0};
+      if (t0 + t < N) {
+        const uint2 src = *reinterpret_cast<const uint2*>(xg + (size_t)t * 128 + c8 * 8);
+        const uint32_t sv[2] = {src.x, src.y};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float f = (float)(int8_t)((sv[e / 4] >> (8 * (e % 4))) & 0xFF);
+          w[e / 2] |= (uint32_t)f32_to_bf16_bits(f) << (16 * (e % 2));
+        }
+      }
+      *reinterpret_cast<uint4*>(sm + kTcX + atom * 16384 + t * 128 + ((ch ^ (t & 7)) << 4)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(sm + kTcH)[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
+        const uint32_t oc = (s / 4) * kpad * 128 + (s % 4) * 32;
+        mma_f16_ss_w(tmem, desc_k_sw128(base + kTcX + o), desc_k_sw128(base + kTcC + oc), ia, s > 0);
+      }
+      mma_commit_w(smem_u32(&bar));
+    }
+    ok = mbar_wait(smem_u32(&bar), phase, &abort_flag, const_cast<int*>(status));
+    phase ^= 1;
+    tc_fence_after();
+    if (warp < 4 && __all_sync(0xffffffffu, ok)) {
+      // one token per thread: its row of D_a
+      const int t = warp * 32 + lane;
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+      int best = 0x7FFFFFFF, bestm = 0;
+      for (int c0 = 0; c0 < kpad; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(trow + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int m = c0 + c;
+          const int dist = cnorm[min(m, 255)] - 2 * (int)__uint_as_float(v[c]);
+          if (m < k && dist < best) { best = dist; bestm = m; }
+        }
+      }
+      if (t0 + t < N) {
+        labels[(size_t)bh * N + t0 + t] = bestm;
+        atomicAdd(&cnt[bestm], 1);
+        // H^T[bestm][t] = 1.0 (bf16), K-major swizzled over the token axis
+        const int atom = t / 64, c8 = (t % 64) / 8, e = t % 8;
+        *reinterpret_cast<uint16_t*>(sm + kTcH + atom * 16384 + bestm * 128 +
+                                     ((c8 ^ (bestm & 7)) << 4) + e * 2) = 0x3F80;
+      }
+    }
+    if (!__syncthreads_and(ok)) break;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_f16_ss_w(tmem + col_u, desc_k_sw128(base + kTcH + (s / 4) * 16384 + (s % 4) * 32),
+                     make_desc(base + kTcX + s * 2048, 16384, 1024, 2), iu, (tt > 0 || s > 0));
+      mma_commit_w(smem_u32(&bar));
+    }
+    ok = mbar_wait(smem_u32(&bar), phase, &abort_flag, const_cast<int*>(status));
+    phase ^= 1;
+    tc_fence_after();
+    ok = __syncthreads_and(ok);
+  }
+  if (ok && ntiles > 0 && warp < 4) {
+    // cluster row m = TMEM lane m of D_u
+    const int m = warp * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + col_u;
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(trow + c0, v);
+      tmem_ld_wait();
+      if (m < k && cnt[m] > 0)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int sv = (int)__uint_as_float(v[c]);
+          if (sv) atomicAdd(&sums[((size_t)bh * k + m) * 128 + c0 + c], sv);
+        }
+    }
+  }
+  __syncthreads();
+  for (int m = tid; m < k; m += 256)
+    if (cnt[m]) atomicAdd(&counts[(size_t)bh * k + m], cnt[m]);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
 // Round-half-even of s / n (n > 0) in exact integer arithmetic.
 __device__ __forceinline__ int div_rne(int s, int n) {
   int q = s / n, r = s % n;
@@ -451,84 +633,84 @@ __global__ void __launch_bounds__(256) quant_k8_kernel(const uint16_t* k, const 
   store64_e4m3(khat + ((size_t)bh * Npad + row) * 128 + h * 64, f, s);
 }
 
-// Gather one channel of one permuted block (zero rows past N).
-__device__ __forceinline__ void gather_channel(const uint16_t* v, const int32_t* perm, int bh,
-                                               int j, int c, int N, float (&x)[128]) {
-#pragma unroll
-  for (int r = 0; r < 128; ++r) {
-    const int row = j * 128 + r;
-    x[r] = row < N ? bf16_bits_to_f32(v[((size_t)bh * N + perm[(size_t)bh * N + row]) * 128 + c])
-                   : 0.0f;
+// Gather the 128 permuted rows of block j (bf16, zero rows past N) into shared
+// memory: 256 threads, coalesced 16-byte loads of whole 256-byte rows.
+__device__ __forceinline__ void gather_block(const uint16_t* v, const int32_t* perm, int bh, int j,
+                                             int N, uint16_t (*tile)[128]) {
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+    const int r = i / 16, c16 = i % 16, row = j * 128 + r;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (row < N)
+      w = *reinterpret_cast<const uint4*>(
+          v + ((size_t)bh * N + perm[(size_t)bh * N + row]) * 128 + c16 * 8);
+    *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = w;
   }
 }
 
-// grid (nb, BH), 128 threads (one per channel): block mean (Eq 4) of V' =
-// V[pi]: fp32 tree sum / n_j, rounded to bf16; residual channel maxima.
-__global__ void __launch_bounds__(128) vpass1_kernel(const uint16_t* v, const int32_t* perm,
+// grid (nb, BH), 256 threads: block mean (Eq 4) of V' = V[pi]: fp32 tree sum
+// over the 128 rows (row r + row r+64, then +32, ...; padded rows 0) / n_j,
+// rounded to bf16; and the per-block residual channel maxima.  Threads
+// 0..127 own one channel each.
+__global__ void __launch_bounds__(256) vpass1_kernel(const uint16_t* v, const int32_t* perm,
                                                      uint16_t* mu, float* vamax, int N, int nb,
                                                      const int* status) {
+  __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
   const int nj = min(128, N - j * 128);
+  gather_block(v, perm, bh, j, N, tile);
+  __syncthreads();
+  if (c >= 128) return;
   float x[128];
-  gather_channel(v, perm, bh, j, c, N, x);
+#pragma unroll
+  for (int r = 0; r < 128; ++r) x[r] = bf16_bits_to_f32(tile[r][c]);
   const float mean = __fdiv_rn(tree128(x), (float)nj);
   const uint16_t m16 = f32_to_bf16_bits(mean);
   const float mf = bf16_bits_to_f32(m16);
-  gather_channel(v, perm, bh, j, c, N, x);  // the tree overwrote x; re-read (cache hits)
   float amax = 0.0f;
-#pragma unroll
-  for (int r = 0; r < 128; ++r)
-    if (r < nj) amax = fmaxf(amax, fabsf(__fsub_rn(x[r], mf)));
+  for (int r = 0; r < nj; ++r) amax = fmaxf(amax, fabsf(__fsub_rn(bf16_bits_to_f32(tile[r][c]), mf)));
   mu[((size_t)bh * nb + j) * 128 + c] = m16;
   vamax[((size_t)bh * nb + j) * 128 + c] = amax;
 }
 
-// grid BH, 128 threads: sv = max over blocks / 448; mutilde = mu / sv; and
-// the mean operand of the restoration MMA (zeroed beforehand).  Blocks form
-// groups of kGroup, aligned to the last block (block j is slot (j + gpad) %
-// kGroup of group (j + gpad) / kGroup); per group two 128 (channel) x 16 (K)
-// bf16 K-major chunks without swizzle, element (c, k) at (c/8)*256 +
-// (k/8)*128 + (c%8)*16 + (k%8)*2: chunk 0 holds bf16(mutilde), chunk 1 the
-// bf16 of the remainder; K columns kGroup..15 and leading empty slots stay 0.
-__global__ void vreduce_kernel(const float* vamax, const uint16_t* mu, float* sv, float* mutilde,
-                               uint8_t* mside, int nb, int ngroups, int gpad, const int* status) {
+// grid BH, 256 threads: sv[c] = (max over blocks of the residual channel
+// maxima) / 448, or 1 for an all-zero channel.
+__global__ void vreduce_kernel(const float* vamax, float* sv, int nb, const int* status) {
+  __shared__ float part[2][128];
   if (prep_skip(status)) return;
-  const int bh = blockIdx.x, c = threadIdx.x;
+  const int bh = blockIdx.x, c = threadIdx.x % 128, half = threadIdx.x / 128;
   float m = 0.0f;
-  for (int j = 0; j < nb; ++j) m = fmaxf(m, vamax[((size_t)bh * nb + j) * 128 + c]);
-  const float s = e4m3_scale(m);
-  sv[(size_t)bh * 128 + c] = s;
-  uint8_t* gbase = mside + (size_t)bh * ngroups * kGroupBytes;
-  const uint32_t coff = (c / 8) * 256 + (c % 8) * 16;
-  for (int j = 0; j < nb; ++j) {
-    const size_t o = ((size_t)bh * nb + j) * 128 + c;
-    const float mt = __fdiv_rn(bf16_bits_to_f32(mu[o]), s);
-    mutilde[o] = mt;
-    const uint16_t hi = f32_to_bf16_bits(mt);
-    const uint16_t lo = f32_to_bf16_bits(__fsub_rn(mt, bf16_bits_to_f32(hi)));
-    const int g = (j + gpad) / kGroup, k = (j + gpad) % kGroup;
-    uint8_t* tile = gbase + (size_t)g * kGroupBytes;
-    const uint32_t off = coff + (k / 8) * 128 + (k % 8) * 2;
-    *reinterpret_cast<uint16_t*>(tile + off) = hi;
-    *reinterpret_cast<uint16_t*>(tile + kGroupBytes / 2 + off) = lo;
-  }
+  for (int j = half; j < nb; j += 2) m = fmaxf(m, vamax[((size_t)bh * nb + j) * 128 + c]);
+  part[half][c] = m;
+  __syncthreads();
+  if (half == 0) sv[(size_t)bh * 128 + c] = e4m3_scale(fmaxf(part[0][c], part[1][c]));
 }
 
-// grid (nb, BH), 128 threads (one per channel): R = V' - mu, R^ = E4M3(R / sv)
-// written transposed (tokens fastest).
-__global__ void __launch_bounds__(128) vpass2_kernel(const uint16_t* v, const int32_t* perm,
+// grid (nb, BH), 256 threads (0..127 own a channel): R = V' - mu, R^ =
+// E4M3(R / sv) written transposed (tokens fastest); mutilde = mu / sv and the
+// mean operand of the restoration MMA.  Blocks form groups of kGroup aligned
+// to the last block (block j is slot (j + gpad) % kGroup of group
+// (j + gpad) / kGroup); per group two 128 (channel) x 16 (K) bf16 K-major
+// chunks without swizzle, element (c, k) at (c/8)*256 + (k/8)*128 + (c%8)*16
+// + (k%8)*2: chunk 0 holds bf16(mutilde), chunk 1 the bf16 of the remainder;
+// the operand is zeroed beforehand, so K columns kGroup..15 and leading empty
+// slots stay 0.
+__global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const int32_t* perm,
                                                      const uint16_t* mu, const float* sv,
-                                                     uint8_t* rhatT, int N, int Npad, int nb,
-                                                     const int* status) {
+                                                     uint8_t* rhatT, float* mutilde,
+                                                     uint8_t* mside, int N, int Npad, int nb,
+                                                     int ngroups, int gpad, const int* status) {
+  __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  float x[128];
-  gather_channel(v, perm, bh, j, c, N, x);
-  const float mf = bf16_bits_to_f32(mu[((size_t)bh * nb + j) * 128 + c]);
+  gather_block(v, perm, bh, j, N, tile);
+  __syncthreads();
+  if (c >= 128) return;
+  const size_t o = ((size_t)bh * nb + j) * 128 + c;
+  const float mf = bf16_bits_to_f32(mu[o]);
   const float s = sv[(size_t)bh * 128 + c];
   uint4* dst = reinterpret_cast<uint4*>(rhatT + ((size_t)bh * 128 + c) * Npad + (size_t)j * 128);
-#pragma unroll
+#pragma unroll 2
   for (int q = 0; q < 8; ++q) {
     uint32_t w[4];
 #pragma unroll
@@ -537,12 +719,21 @@ __global__ void __launch_bounds__(128) vpass2_kernel(const uint16_t* v, const in
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int r = q * 16 + e * 4 + u;
-        y[u] = (j * 128 + r < N) ? __fdiv_rn(__fsub_rn(x[r], mf), s) : 0.0f;
+        y[u] = (j * 128 + r < N) ? __fdiv_rn(__fsub_rn(bf16_bits_to_f32(tile[r][c]), mf), s) : 0.0f;
       }
       w[e] = (uint32_t)f32x2_to_e4m3x2(y[0], y[1]) | ((uint32_t)f32x2_to_e4m3x2(y[2], y[3]) << 16);
     }
     dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  const float mt = __fdiv_rn(mf, s);
+  mutilde[o] = mt;
+  const uint16_t hi = f32_to_bf16_bits(mt);
+  const uint16_t lo = f32_to_bf16_bits(__fsub_rn(mt, bf16_bits_to_f32(hi)));
+  const int g = (j + gpad) / kGroup, k = (j + gpad) % kGroup;
+  uint8_t* tile_g = mside + ((size_t)bh * ngroups + g) * kGroupBytes;
+  const uint32_t off = (c / 8) * 256 + (c % 8) * 16 + (k / 8) * 128 + (k % 8) * 2;
+  *reinterpret_cast<uint16_t*>(tile_g + off) = hi;
+  *reinterpret_cast<uint16_t*>(tile_g + kGroupBytes / 2 + off) = lo;
 }
 
 inline int grid_chunks(size_t work, int per_block, int cap) {
@@ -580,15 +771,29 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
     head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, per_head, status);
     features_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
     kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
-    const int groups = k <= 96 ? 2 : 1;
-    const size_t asmem = assign_smem_bytes(k, groups);
-    cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)asmem);
-    const int tiles = (N + kAssignTokens - 1) / kAssignTokens;
-    for (int it = 0; it < a.iters; ++it) {
-      kmeans_assign_kernel<<<dim3(tiles, BH), 256, asmem, st>>>(x, cent, labels, sums, counts, N,
-                                                                k, groups, status);
-      kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
+    if (k <= 128) {
+      // tensor-core Lloyd iteration (the cluster-sum product has M = 128 rows)
+      const int kpad = (k + 15) / 16 * 16;
+      const size_t tsmem = kmeans_tc_smem_bytes(kpad);
+      cudaFuncSetAttribute(kmeans_assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tsmem);
+      const int tiles = ((N + 127) / 128 + kTcTiles - 1) / kTcTiles;
+      for (int it = 0; it < a.iters; ++it) {
+        kmeans_assign_tc_kernel<<<dim3(tiles, BH), 256, tsmem, st>>>(x, cent, labels, sums,
+                                                                     counts, N, k, kpad, status);
+        kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
+      }
+    } else {
+      const int groups = k <= 96 ? 2 : 1;
+      const size_t asmem = assign_smem_bytes(k, groups);
+      cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)asmem);
+      const int tiles = (N + kAssignTokens - 1) / kAssignTokens;
+      for (int it = 0; it < a.iters; ++it) {
+        kmeans_assign_kernel<<<dim3(tiles, BH), 256, asmem, st>>>(x, cent, labels, sums, counts,
+                                                                  N, k, groups, status);
+        kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
+      }
     }
     // stable counting sort; the k-means sums buffer is reused for the histogram
     const int nchunk = (N + kSortChunk - 1) / kSortChunk;
@@ -614,13 +819,13 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
   key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
   quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
-  vpass1_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
   const int ngroups = (nb + kGroup - 1) / kGroup;
   zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroupBytes / 4, 256, 4096), 256, 0, st>>>(
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroupBytes / 4);
-  vreduce_kernel<<<BH, 128, 0, st>>>(vamax, mu, sv, mut, mside, nb, ngroups,
-                                     ngroups * kGroup - nb, status);
-  vpass2_kernel<<<dim3(nb, BH), 128, 0, st>>>(v, perm, mu, sv, rhatT, N, Npad, nb, status);
+  vpass2_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, sv, rhatT, mut, mside, N, Npad, nb,
+                                              ngroups, ngroups * kGroup - nb, status);
   header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
