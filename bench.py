@@ -35,6 +35,14 @@ METRIC = "attention TFLOPS & % of GB300 FP8 tensor peak at N=75600,H=40,d=128; V
 FP8_NOMINAL_TFLOPS = 4500.0   # dense FP8 per GPU (NVIDIA nominal)
 FP8_PER_BF16 = 2.0            # nominal FP8 : BF16 dense ratio
 
+# DRAM bytes (read + write) of one FP8 attention launch, from one ncu capture
+# of the sweep16k workload (B1 H24 N16384): 154.6 MB read + 70.0 MB written.
+# Every row of Q, K, R and O crosses DRAM once, so the figure scales with the
+# token count.  It holds only for the kernel source it was captured on.
+ATTN_TRAFFIC = dict(bytes=154.639104e6 + 69.965568e6, tokens=24 * 16384,
+                    sources={"attn_fp8.cu": "d7f0ef868e92f6c2375a39a9a5ddb5ed2204053767769bd774274cda81f2a72e",
+                             "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"})
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -44,6 +52,38 @@ def peaks():
         return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
                     bf16_sus=float(m["bf16_tflops_sustained"]), src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def attn_traffic(w):
+    """Scaled DRAM traffic of one attention launch, or None if the kernel
+    source differs from the one the counters were taken on."""
+    import hashlib
+    csrc = os.path.join(ROOT, "bit_attention_video_gb300", "csrc")
+    for name, digest in ATTN_TRAFFIC["sources"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    if w.bits != 8:
+        return None
+    return ATTN_TRAFFIC["bytes"] * (w.B * w.H * w.N) / ATTN_TRAFFIC["tokens"]
+
+
+def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
+    """Algorithmic DRAM bytes of one V-Smooth preparation (8-bit): read Q, K,
+    V (bf16) once for the quantisers and V once more for the grouping
+    features; write the int8 features, read them once per Lloyd iteration;
+    write the E4M3 codes of Q, K and R^T, the permutation, the block means
+    (bf16 and fp32) and the per-block scales."""
+    BH, N, d = w.B * w.H, w.N, w.d
+    nb = (N + 127) // 128
+    npad = nb * 128
+    total = 3 * BH * N * d * 2 + 3 * BH * npad * d + BH * nb * d * (2 + 4) + BH * nb * 8
+    total += 4 * BH * N * 2                     # permutation: written, read by the gathers
+    if not reuse:
+        total += BH * N * d * 2                 # V read by the feature pass
+        total += BH * N * d * (1 + iters)       # int8 features: written once, read per iteration
+        total += 4 * BH * N * iters             # labels written per iteration
+    return float(total)
 
 
 def launches_per_step(iters: int, reuse: bool) -> int:
@@ -294,11 +334,13 @@ def run_gpu(args, w):
         "pct_fp8_peak": 100.0 * attn_tflops / fp8_peak,
         "pct_fp8_nominal": 100.0 * attn_tflops / FP8_NOMINAL_TFLOPS,
         "vsmooth_ms": statistics.mean(prep_ms),
-        "vsmooth_gbs": None,
+        "vsmooth_gbs": vsmooth_bytes(w, args.iters, args.reuse) / (statistics.mean(prep_ms) * 1e-3)
+        / 1e9,
+        "vsmooth_bytes": vsmooth_bytes(w, args.iters, args.reuse),
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": attn_tflops / fp8_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": attn_tflops / fp8_peak, "traffic": attn_traffic(w),
                      "kernel": "attn_fp8_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x {FP8_PER_BF16} "
                                  "(nominal FP8:BF16 ratio)"},
