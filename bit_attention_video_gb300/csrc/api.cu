@@ -36,14 +36,14 @@ int compute_layout(int B, int H, int N, int d, int k, int bits, vca_state_layout
     L->mutilde = take(BH * nb * d * 4);
   } else {
     L->q4 = take(BH * Npad * d / 2);
-    L->q4s = take(BH * Npad * d / 16);
+    L->q4s = take(BH * nb * kScaleTileBytes);
     L->k4 = take(BH * Npad * d / 2);
-    L->k4s = take(BH * Npad * d / 16);
+    L->kr4s = take(BH * nb * 2 * kScaleTileBytes);
     L->r4T = take(BH * d * Npad / 2);
-    L->r4s = take(BH * d * Npad / 16);
     L->g4 = take(BH * 16);
   }
-  L->mside = take(BH * ((nb + kGroup - 1) / kGroup) * kGroupBytes);
+  L->mside = bits == 8 ? take(BH * ((nb + kGroup - 1) / kGroup) * kGroupBytes)
+                       : take(BH * ((nb + kGroup4 - 1) / kGroup4) * kGroup4Bytes);
   L->mu = take(BH * nb * d * 2);
   L->kbar = take(BH * d * 2);
   L->perm = take(BH * N * 4);
@@ -64,7 +64,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
-                  uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1) {
+                  uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+                  bool swizzle64) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* p = nullptr;
@@ -82,7 +83,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d
   const CUtensorMapDataType dt =
       elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -239,6 +239,31 @@ __device__ __forceinline__ void mma_f16_ts_w(uint32_t d, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
 }
+// kind::mxf4nvf4 block-scaled product (NVFP4): E2M1 x E2M1 -> f32 with one
+// UE4M3 scale per 16 elements along K (scale_vec::4X: four scales per row for
+// the K = 64 of one instruction).  Both operands come from shared memory; the
+// scale factors of A and B sit in tensor memory (`sfa`, `sfb`).
+__device__ __forceinline__ void mma_nvf4_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nelect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\n"
+      "@p tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%5], [%6], q;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory (a no-swizzle K-major matrix,
+// rows 16 bytes apart) into tensor memory columns [col, col+4), replicated
+// into all four 32-lane quarters.  This is how block scale factors reach the
+// tensor core: for a 128-row operand, lane l, column col+i holds the four
+// scales of row 32 i + l.  Ordered with the MMAs the same thread issues.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_w(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\n"
+      "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\n"
@@ -266,10 +291,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::mxf4nvf4 (block-scaled, f32 accumulator):
+//   bits 4-5 B scale-factor id (0), 7-9 A format, 10-12 B format (E2M1 = 1),
+//   15 / 16 A / B major (K-major only), 17-22 N>>3, 23 scale format
+//   (0 = UE4M3), 24-28 M>>4, 29-30 A scale-factor id (0).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (0u << 23) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor (tcgen05 form):
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout
-//   (0 = no swizzle, 2 = 128-byte swizzle).
+//   (0 = no swizzle, 2 = 128-byte swizzle, 4 = 64-byte swizzle).
 __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                               uint32_t layout) {
   uint64_t d = 0;
@@ -284,6 +318,15 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
 // (the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes).
 __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr) {
   return make_desc(saddr, 16, 1024, 2);
+}
+// K-major tile of rows x 64 bytes, 64-byte swizzle, 8-row atoms of 512 B
+// (the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_64B writes).
+__device__ __forceinline__ uint64_t desc_k_sw64(uint32_t saddr) {
+  return make_desc(saddr, 16, 512, 4);
+}
+// Byte offset of 16-byte chunk `c` (0..3) of row `r` in that layout.
+__device__ __forceinline__ uint32_t off_sw64(int r, int c) {
+  return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((c ^ ((r & 7) >> 1)) << 4));
 }
 // K-major, no swizzle: 8x16-byte core matrices; `lbo` steps along K, `sbo`
 // steps along M/N.

@@ -101,6 +101,27 @@ __global__ void __launch_bounds__(128, 1)
       *reinterpret_cast<uint16_t*>(sm + (B2 - base) + off_k_plain(r, k, 2, 128, 256)) = bs[i];
     }
   }
+  // Mode 7 (NVFP4): a and b each hold [128][64] packed E2M1 bytes (element 2i
+  // in the low nibble) and then [128][8] UE4M3 scales, one per 16 elements.
+  // Operands go to the 64-byte-swizzled K-major layout; the scales to the
+  // layout the scale copy reads: for K step s, 512 bytes where row m, block
+  // kb (of that step's four) sits at (m % 32) * 16 + (m / 32) * 4 + kb.
+  constexpr uint32_t kSfA = 32768, kSfB = 33792;
+  if (mode == 7) {
+    for (int i = tid; i < 128 * 4; i += 128) {
+      const int r = i / 4, c = i % 4;
+      *reinterpret_cast<uint4*>(sm + (A - base) + off_sw64(r, c)) =
+          *reinterpret_cast<const uint4*>(a + r * 64 + c * 16);
+      *reinterpret_cast<uint4*>(sm + (B - base) + off_sw64(r, c)) =
+          *reinterpret_cast<const uint4*>(b + r * 64 + c * 16);
+    }
+    for (int i = tid; i < 128 * 8; i += 128) {
+      const int m = i / 8, kb = i % 8;
+      const uint32_t o = (kb / 4) * 512 + (m % 32) * 16 + (m / 32) * 4 + kb % 4;
+      sm[(A - base) + kSfA + o] = a[8192 + i];
+      sm[(A - base) + kSfB + o] = b[8192 + i];
+    }
+  }
   fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
@@ -129,7 +150,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (tid == 0) {
+  if (tid == 0 && mode != 7) {
     const uint32_t i8 = idesc_f8(128, 128), i16 = idesc_bf16(128, 128),
                    i16mn = idesc_bf16(128, 128, true);
     if (mode == 0 || mode == 6)
@@ -158,6 +179,17 @@ __global__ void __launch_bounds__(128, 1)
       for (int s = 0; s < 4; ++s)
         mma_f8_ts(tmem, tmem + 128 + 8 * s, desc_k_sw128(B + 32 * s), i8, s > 0);
     mma_commit(smem_u32(&bar));
+  }
+  if (mode == 7 && warp == 0) {
+    // scale factors: A in columns 128.., B in columns 160.., four per K step
+    for (int s = 0; s < 2; ++s) {
+      tmem_cp_32x128b_x4_w(tmem + 128 + 4 * s, desc_k_plain(A + kSfA + 512 * s, 512, 128));
+      tmem_cp_32x128b_x4_w(tmem + 160 + 4 * s, desc_k_plain(A + kSfB + 512 * s, 512, 128));
+    }
+    for (int s = 0; s < 2; ++s)
+      mma_nvf4_ss_w(tmem, desc_k_sw64(A + 32 * s), desc_k_sw64(B + 32 * s), idesc_nvf4(128, 128),
+                    tmem + 128 + 4 * s, tmem + 160 + 4 * s, s > 0);
+    mma_commit_w(smem_u32(&bar));
   }
   __syncwarp();
   const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, status);
@@ -201,7 +233,7 @@ extern "C" int vca_debug_encode(const float* x, uint8_t* e4, uint8_t* e2, size_t
 
 extern "C" int vca_debug_mma(int mode, const void* a, const void* b, float* d,
                              vca_stream_t stream) {
-  if (mode < 0 || mode > 6 || !a || !b || !d) return VCA_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 7 || !a || !b || !d) return VCA_ERR_INVALID_ARG;
   if (cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kDbgSmem + 1024) != cudaSuccess)
     return VCA_ERR_CUDA;

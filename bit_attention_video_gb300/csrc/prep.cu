@@ -736,6 +736,190 @@ __global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const in
   *reinterpret_cast<uint16_t*>(tile_g + kGroupBytes / 2 + off) = lo;
 }
 
+// ---------------------------------------------------------------------------
+// Quantizers (4-bit, NVFP4; Appx B "At 4 bits the NVFP4 microscales ...")
+// ---------------------------------------------------------------------------
+// Per-head NVFP4 global scale: amax / (448 * 6), so the largest 16-block gets
+// the largest UE4M3 scale and its E2M1 elements reach 6; 1 for a zero tensor.
+__device__ __forceinline__ float nvfp4_global(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+}
+
+// 16 values under global scale g: block scale UE4M3(amax / (6 g)) (returned),
+// elements E2M1(x / (scale g)) packed into 8 bytes (element 2i low nibble).
+__device__ __forceinline__ uint32_t nvfp4_16(const float* x, float g, uint2& packed) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
+  const uint32_t sc = f32_to_e4m3(__fdiv_rn(m, __fmul_rn(6.0f, g)));
+  const float scv = e4m3_to_f32((uint8_t)sc);
+  uint32_t w[2] = {0u, 0u};
+  if (scv > 0.0f) {
+    const float step = __fmul_rn(scv, g);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2)
+      w[i / 8] |= (uint32_t)f32x2_to_e2m1x2(__fdiv_rn(x[i], step), __fdiv_rn(x[i + 1], step))
+                  << (4 * (i % 8));
+  }
+  packed = make_uint2(w[0], w[1]);
+  return sc;
+}
+
+// Byte offset of the scales of row m, blocks 4s..4s+3, in a 1024-byte scale
+// tile (the order the tensor core reads: (kb/4)*512 + (m%32)*16 + (m/32)*4 + kb%4).
+__device__ __forceinline__ uint32_t scale_tile_off(int m, int s) {
+  return (uint32_t)(s * 512 + (m % 32) * 16 + (m / 32) * 4);
+}
+
+// 64 values of a row (channels 64h..64h+63): four NVFP4 blocks, 32 code bytes
+// to `dst` and the four scale bytes (one word) to `sdst`.
+__device__ __forceinline__ void store64_nvfp4(const float (&f)[64], float g, uint8_t* dst,
+                                              uint8_t* sdst) {
+  uint32_t sc4 = 0;
+  uint2 pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sc4 |= nvfp4_16(&f[16 * i], g, pk[i]) << (8 * i);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(pk[0].x, pk[0].y, pk[1].x, pk[1].y);
+  d[1] = make_uint4(pk[2].x, pk[2].y, pk[3].x, pk[3].y);
+  *reinterpret_cast<uint32_t*>(sdst) = sc4;
+}
+
+// grid (chunks, BH): max |K - kbar| of each head (the set of K' rows does not
+// depend on the order), as the uint bits of a non-negative float.
+__global__ void k4_amax_kernel(const uint16_t* k, const uint16_t* kbar, uint32_t* amax_bits,
+                               size_t per_head, const int* status) {
+  __shared__ float red[32];
+  if (prep_skip(status)) return;
+  const size_t bh = blockIdx.y;
+  const uint4* src = reinterpret_cast<const uint4*>(k + bh * per_head);
+  const uint16_t* kb = kbar + bh * 128;
+  const size_t n8 = per_head / 8;
+  float m = 0.0f;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 w = src[i];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    const int c0 = (int)((i * 8) % 128);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      m = fmaxf(m, fabsf(__fsub_rn(__uint_as_float(ws[e] << 16), bf16_bits_to_f32(kb[c0 + 2 * e]))));
+      m = fmaxf(m, fabsf(__fsub_rn(__uint_as_float(ws[e] & 0xFFFF0000u),
+                                   bf16_bits_to_f32(kb[c0 + 2 * e + 1]))));
+    }
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
+}
+
+// grid BH, 256 threads: the three global scales gq, gk, gr of a head (gr from
+// the per-block residual channel maxima).
+__global__ void g4_kernel(const uint32_t* amax_q, const uint32_t* amax_k, const float* vamax,
+                          float* g4, int nb, const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x;
+  float m = 0.0f;
+  for (size_t i = threadIdx.x; i < (size_t)nb * 128; i += 256)
+    m = fmaxf(m, vamax[(size_t)bh * nb * 128 + i]);
+  m = block_max(m, red);
+  if (threadIdx.x == 0) {
+    g4[bh * 4 + 0] = nvfp4_global(__uint_as_float(amax_q[bh]));
+    g4[bh * 4 + 1] = nvfp4_global(__uint_as_float(amax_k[bh]));
+    g4[bh * 4 + 2] = nvfp4_global(m);
+    g4[bh * 4 + 3] = 0.0f;
+  }
+}
+
+// grid (nb, BH), 256 threads: Q in NVFP4, blocks of 16 along d.  Thread t
+// covers row t/2, channels 64*(t%2) ...
+__global__ void __launch_bounds__(256) quant_q4_kernel(const uint16_t* q, const float* g4,
+                                                       uint8_t* q4, uint8_t* q4s, int N, int Npad,
+                                                       int nb, const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
+  float f[64];
+  if (row < N) {
+    load64(q + ((size_t)bh * N + row) * 128 + h * 64, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  }
+  store64_nvfp4(f, g4[bh * 4 + 0], q4 + ((size_t)bh * Npad + row) * 64 + h * 32,
+                q4s + ((size_t)bh * nb + j) * kScaleTileBytes + scale_tile_off(r, h));
+}
+
+// grid (nb, BH), 256 threads: K' = K[pi] - kbar in NVFP4, blocks of 16 along d;
+// scales into the first tile of the block's K'/R scale pair.
+__global__ void __launch_bounds__(256) quant_k4_kernel(const uint16_t* k, const int32_t* perm,
+                                                       const uint16_t* kbar, const float* g4,
+                                                       uint8_t* k4, uint8_t* kr4s, int N,
+                                                       int Npad, int nb, const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
+  float f[64];
+  if (row < N) {
+    const int src = perm[(size_t)bh * N + row];
+    load64(k + ((size_t)bh * N + src) * 128 + h * 64, f);
+    const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  }
+  store64_nvfp4(f, g4[bh * 4 + 1], k4 + ((size_t)bh * Npad + row) * 64 + h * 32,
+                kr4s + ((size_t)bh * nb + j) * 2 * kScaleTileBytes + scale_tile_off(r, h));
+}
+
+// grid (nb, BH), 256 threads (0..127 own a channel): R = V' - mu in NVFP4,
+// blocks of 16 tokens, written transposed (tokens fastest) with the scales in
+// the second tile of the block's K'/R scale pair; and the block mean into the
+// 4-bit mean operand (group (j + gpad) / 4, slot u = (j + gpad) % 4, K rows
+// 2u, 2u+1, 8+2u, 9+2u; element (c, k) at (c/8)*256 + (k/8)*128 + (c%8)*16 +
+// (k%8)*2; zeroed beforehand, so empty leading slots stay 0).
+__global__ void __launch_bounds__(256) vpass2_4_kernel(const uint16_t* v, const int32_t* perm,
+                                                       const uint16_t* mu, const float* g4,
+                                                       uint8_t* r4T, uint8_t* kr4s,
+                                                       uint8_t* mside, int N, int Npad, int nb,
+                                                       int ngroups, int gpad, const int* status) {
+  __shared__ __align__(16) uint16_t tile[128][128];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  gather_block(v, perm, bh, j, N, tile);
+  __syncthreads();
+  if (c >= 128) return;
+  const size_t o = ((size_t)bh * nb + j) * 128 + c;
+  const uint16_t m16 = mu[o];
+  const float mf = bf16_bits_to_f32(m16);
+  const float g = g4[bh * 4 + 2];
+  uint8_t* dst = r4T + ((size_t)bh * 128 + c) * (Npad / 2) + (size_t)j * 64;
+  uint32_t sc[2] = {0u, 0u};
+#pragma unroll 1
+  for (int kb = 0; kb < 8; ++kb) {
+    float x[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int r = kb * 16 + u;
+      x[u] = (j * 128 + r < N) ? __fsub_rn(bf16_bits_to_f32(tile[r][c]), mf) : 0.0f;
+    }
+    uint2 pk;
+    sc[kb / 4] |= nvfp4_16(x, g, pk) << (8 * (kb % 4));
+    *reinterpret_cast<uint2*>(dst + kb * 8) = pk;
+  }
+  uint8_t* st = kr4s + ((size_t)bh * nb + j) * 2 * kScaleTileBytes + kScaleTileBytes;
+  *reinterpret_cast<uint32_t*>(st + scale_tile_off(c, 0)) = sc[0];
+  *reinterpret_cast<uint32_t*>(st + scale_tile_off(c, 1)) = sc[1];
+  const int grp = (j + gpad) / kGroup4, u = (j + gpad) % kGroup4;
+  uint8_t* tg = mside + ((size_t)bh * ngroups + grp) * kGroup4Bytes + (c / 8) * 256 + (c % 8) * 16;
+  const int ks[4] = {2 * u, 2 * u + 1, 8 + 2 * u, 9 + 2 * u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint16_t*>(tg + (ks[i] / 8) * 128 + (ks[i] % 8) * 2) = m16;
+}
+
 inline int grid_chunks(size_t work, int per_block, int cap) {
   return (int)std::max<size_t>(1, std::min<size_t>((work + per_block - 1) / per_block, cap));
 }
@@ -745,20 +929,21 @@ inline int grid_chunks(size_t work, int per_block, int cap) {
 // ---------------------------------------------------------------------------
 // host: the preparation chain
 // ---------------------------------------------------------------------------
-int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
-  const int BH = a.B * a.H, N = a.N, nb = a.nb, Npad = a.Npad, k = a.k;
+// Header, grouping (skipped when the cached permutation is reused) and the
+// key channel mean: the part of the chain both bit widths share.
+static void launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
+  const int BH = a.B * a.H, N = a.N, nb = a.nb, k = a.k;
   const size_t per_head = (size_t)N * 128;
   uint8_t* S = a.state;
   const vca_state_layout& L = a.L;
   int* status = reinterpret_cast<int*>(S + L.status);
   uint32_t* hdr = reinterpret_cast<uint32_t*>(S + L.header);
-  const uint16_t* q = a.q;
   const uint16_t* kk = a.k_in;
   const uint16_t* v = a.v;
   int32_t* labels = reinterpret_cast<int32_t*>(S + L.labels);
   int32_t* perm = reinterpret_cast<int32_t*>(S + L.perm);
 
-  header_kernel<<<1, 32, 0, st>>>(hdr, status, a.B, a.H, N, 128, k, 8, a.reuse);
+  header_kernel<<<1, 32, 0, st>>>(hdr, status, a.B, a.H, N, 128, k, bits, a.reuse);
   if (!a.reuse) {
     uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + L.grid);
     float* gscale = reinterpret_cast<float*>(S + L.grid) + BH;
@@ -803,12 +988,28 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
     sort_scatter_kernel<<<dim3(nchunk, BH), 256, 0, st>>>(labels, hist, perm, N, k, nchunk,
                                                           status);
   }
+  uint16_t* kbar = reinterpret_cast<uint16_t*>(S + L.kbar);
+  float* ksum = reinterpret_cast<float*>(S + L.ksum);
+  key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
+  key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
+}
+
+int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
+  const int BH = a.B * a.H, N = a.N, nb = a.nb, Npad = a.Npad;
+  uint8_t* S = a.state;
+  const vca_state_layout& L = a.L;
+  int* status = reinterpret_cast<int*>(S + L.status);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(S + L.header);
+  const uint16_t* q = a.q;
+  const uint16_t* kk = a.k_in;
+  const uint16_t* v = a.v;
+  const int32_t* perm = reinterpret_cast<const int32_t*>(S + L.perm);
+  launch_front(a, 8, st);
   uint8_t* qhat = S + L.qhat;
   float* sq = reinterpret_cast<float*>(S + L.sq);
   uint8_t* khat = S + L.khat;
   float* sk = reinterpret_cast<float*>(S + L.sk);
-  uint16_t* kbar = reinterpret_cast<uint16_t*>(S + L.kbar);
-  float* ksum = reinterpret_cast<float*>(S + L.ksum);
+  const uint16_t* kbar = reinterpret_cast<const uint16_t*>(S + L.kbar);
   uint8_t* rhatT = S + L.rhatT;
   float* sv = reinterpret_cast<float*>(S + L.sv);
   uint16_t* mu = reinterpret_cast<uint16_t*>(S + L.mu);
@@ -816,8 +1017,6 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   uint8_t* mside = S + L.mside;
   float* vamax = reinterpret_cast<float*>(S + L.vamax);
   quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
-  key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
-  key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
   quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
   vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, status);
   vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
@@ -826,6 +1025,44 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroupBytes / 4);
   vpass2_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, sv, rhatT, mut, mside, N, Npad, nb,
                                               ngroups, ngroups * kGroup - nb, status);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
+  const int BH = a.B * a.H, N = a.N, nb = a.nb, Npad = a.Npad;
+  const size_t per_head = (size_t)N * 128;
+  uint8_t* S = a.state;
+  const vca_state_layout& L = a.L;
+  int* status = reinterpret_cast<int*>(S + L.status);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(S + L.header);
+  const uint16_t* q = a.q;
+  const uint16_t* kk = a.k_in;
+  const uint16_t* v = a.v;
+  const int32_t* perm = reinterpret_cast<const int32_t*>(S + L.perm);
+  launch_front(a, 4, st);
+  const uint16_t* kbar = reinterpret_cast<const uint16_t*>(S + L.kbar);
+  uint16_t* mu = reinterpret_cast<uint16_t*>(S + L.mu);
+  float* vamax = reinterpret_cast<float*>(S + L.vamax);
+  float* g4 = reinterpret_cast<float*>(S + L.g4);
+  uint8_t* mside = S + L.mside;
+  // per-head |Q| and |K'| maxima in the key-sum scratch (free after the key mean)
+  uint32_t* amax_q = reinterpret_cast<uint32_t*>(S + L.ksum);
+  uint32_t* amax_k = amax_q + BH;
+  zero_kernel<<<1, 256, 0, st>>>(amax_q, 2 * (size_t)BH);
+  const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
+  head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
+  k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  g4_kernel<<<BH, 256, 0, st>>>(amax_q, amax_k, vamax, g4, nb, status);
+  quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, status);
+  quant_k4_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, S + L.k4, S + L.kr4s, N, Npad,
+                                                nb, status);
+  const int ngroups = (nb + kGroup4 - 1) / kGroup4;
+  zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroup4Bytes / 4, 256, 4096), 256, 0, st>>>(
+      reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroup4Bytes / 4);
+  vpass2_4_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, g4, S + L.r4T, S + L.kr4s, mside, N,
+                                                Npad, nb, ngroups, ngroups * kGroup4 - nb, status);
   header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }

@@ -15,6 +15,14 @@ constexpr uint32_t kTileBytes = 128 * 128;         // one 128 x 128 E4M3 tile
 // of the group is K column k, columns kGroup..15 are zero.
 constexpr int kGroup = 8;
 constexpr uint32_t kGroupBytes = 2 * 128 * 16 * 2;
+// 4-bit path: groups of kGroup4 blocks share one 128 (channel) x 16 (K) bf16
+// K-major chunk without swizzle; K row k holds the block mean of slot
+// (k % 8) / 2, so that each softmax thread's row-sum pair (hi, lo) of every
+// slot meets its block's mean.
+constexpr int kGroup4 = 4;
+constexpr uint32_t kGroup4Bytes = 128 * 16 * 2;
+constexpr uint32_t kTile4Bytes = 128 * 64;         // one 128 x 128 E2M1 tile
+constexpr uint32_t kScaleTileBytes = 1024;         // UE4M3 scales of a 128 x 128 tile
 
 // Header words (uint32): magic, B, H, N, d, k, bits, perm cached, operands ready.
 
@@ -42,8 +50,10 @@ int launch_attention_bf16(const void* q, const void* k, const void* v, int B, in
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 // 2-D tensor of `elem_bytes`-byte elements: inner extent `dim0`, `dim1` rows of
-// `row_bytes` bytes, box (box0, box1), 128-byte swizzle.
+// `row_bytes` bytes, box (box0, box1), 128-byte swizzle (64-byte when
+// `swizzle64`).
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
-                  uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1);
+                  uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+                  bool swizzle64 = false);
 
 }  // namespace vca

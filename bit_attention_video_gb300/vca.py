@@ -35,7 +35,7 @@ class StateLayout(C.Structure):
     _fields_ = [(n, C.c_uint64) for n in (
         "total_bytes", "header", "status", "labels", "perm", "centroids", "grid", "features",
         "sums", "qhat", "sq", "khat", "sk", "kbar", "ksum", "rhatT", "sv", "mu", "mutilde",
-        "mside", "vamax", "q4", "q4s", "k4", "k4s", "r4T", "r4s", "g4")]
+        "mside", "vamax", "q4", "q4s", "k4", "kr4s", "r4T", "g4")]
 
 
 def lib():
@@ -177,6 +177,13 @@ def debug_mma(mode, a, b, d, stream=None):
 
 
 # ----------------------------------------------------------------------------
+def scale_tile_to_rows(tile):
+    """A 1024-byte scale tile (tensor-core order) as a [128 rows][8 blocks] array."""
+    t = tile.reshape(*tile.shape[:-1], 2, 32, 4, 4)          # [kb/4][m%32][m/32][kb%4]
+    n = t.dim()
+    return t.permute(*range(n - 4), n - 2, n - 3, n - 4, n - 1).reshape(*tile.shape[:-1], 128, 8)
+
+
 def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
     """Typed views of the arrays of a prepared state blob (for inspection)."""
     B, H, N, d = shape
@@ -194,12 +201,12 @@ def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
         centroids=v(L.centroids, BH * k_clusters * d, torch.int8, (BH, k_clusters, d)),
         kbar=v(L.kbar, BH * d, torch.int16, (BH, d)),
         mu=v(L.mu, BH * nb * d, torch.int16, (BH, nb, d)),
-        mside=v(L.mside, BH * ((nb + 7) // 8) * 4096, torch.int16,
-                (BH, (nb + 7) // 8, 2, 2048)),
         status=v(L.status, 1, torch.int32, (1,)),
     )
     if bits == 8:
         out.update(
+            mside=v(L.mside, BH * ((nb + 7) // 8) * 4096, torch.int16,
+                    (BH, (nb + 7) // 8, 2, 2048)),
             qhat=v(L.qhat, BH * Npad * d, torch.uint8, (BH, Npad, d)),
             sq=v(L.sq, BH * nb, torch.float32, (BH, nb)),
             khat=v(L.khat, BH * Npad * d, torch.uint8, (BH, Npad, d)),
@@ -210,12 +217,13 @@ def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
         )
     else:
         out.update(
+            mside=v(L.mside, BH * ((nb + 3) // 4) * 2048, torch.int16,
+                    (BH, (nb + 3) // 4, 2048)),
             q4=v(L.q4, BH * Npad * d // 2, torch.uint8, (BH, Npad, d // 2)),
-            q4s=v(L.q4s, BH * Npad * d // 16, torch.uint8, (BH, Npad, d // 16)),
+            q4s=v(L.q4s, BH * nb * 1024, torch.uint8, (BH, nb, 1024)),
             k4=v(L.k4, BH * Npad * d // 2, torch.uint8, (BH, Npad, d // 2)),
-            k4s=v(L.k4s, BH * Npad * d // 16, torch.uint8, (BH, Npad, d // 16)),
+            kr4s=v(L.kr4s, BH * nb * 2048, torch.uint8, (BH, nb, 2, 1024)),
             r4T=v(L.r4T, BH * d * Npad // 2, torch.uint8, (BH, d, Npad // 2)),
-            r4s=v(L.r4s, BH * d * Npad // 16, torch.uint8, (BH, d, Npad // 16)),
             g4=v(L.g4, BH * 4, torch.float32, (BH, 4)),
         )
     return out

@@ -75,16 +75,22 @@ typedef struct {
   uint64_t sv;        /* fp32  [BH][d]     per-channel residual scales */
   uint64_t mu;        /* bf16  [BH][nb][d] block means (unscaled) */
   uint64_t mutilde;   /* fp32  [BH][nb][d] mu / sv */
-  uint64_t mside;     /* bf16  [BH][ceil(nb/8)][2][128*16] mean operand of the restoration MMA */
+  uint64_t mside;     /* bf16 mean operand of the restoration MMA: 8-bit
+                       * [BH][ceil(nb/8)][2][128*16]; 4-bit [BH][ceil(nb/4)][128*16] */
   uint64_t vamax;     /* fp32  [BH][nb][d] per-block residual channel maxima (scratch) */
-  /* 4-bit (NVFP4) path */
+  /* 4-bit (NVFP4) path.  E2M1 codes are packed two per byte, element 2i in the
+   * low nibble.  Scale tiles (UE4M3, one per 16 elements along the product's
+   * reduction dimension) cover 128 rows x 8 blocks in 1024 bytes: the scale
+   * of row m, block kb sits at (kb/4)*512 + (m%32)*16 + (m/32)*4 + kb%4, the
+   * order the tensor core reads scale factors in. */
   uint64_t q4;        /* e2m1 packed [BH][Npad][d/2] */
-  uint64_t q4s;       /* ue4m3 [BH][Npad][d/16] */
-  uint64_t k4;        /* e2m1 packed [BH][Npad][d/2] */
-  uint64_t k4s;       /* ue4m3 [BH][Npad][d/16] */
-  uint64_t r4T;       /* e2m1 packed [BH][d][Npad/2] */
-  uint64_t r4s;       /* ue4m3 [BH][d][Npad/16] */
-  uint64_t g4;        /* fp32 [BH][4] global scales gq, gk, gr, - */
+  uint64_t q4s;       /* ue4m3 [BH][nb][1024] scale tile per 128 query rows (blocks along d) */
+  uint64_t k4;        /* e2m1 packed [BH][Npad][d/2] permuted, centred keys */
+  uint64_t kr4s;      /* ue4m3 [BH][nb][2][1024] per key block: the K' scale tile (rows =
+                       * keys, blocks along d), then the R scale tile (rows = channels,
+                       * blocks of 16 tokens) */
+  uint64_t r4T;       /* e2m1 packed [BH][d][Npad/2] residual codes, tokens fastest */
+  uint64_t g4;        /* fp32 [BH][4] global scales gq, gk, gr, 0 */
 } vca_state_layout;
 
 /* Size in bytes of the state blob for this problem (0 if the arguments are
@@ -187,9 +193,12 @@ int vca_debug_encode(const float* x, uint8_t* out_e4m3, uint8_t* out_e2m1, size_
  * 128B-swizzle (K=128); 2 BF16 with B MN-major 128B-swizzle (K=64);
  * 3 BF16 K-major no-swizzle (K=16); 4 BF16 with A in tensor memory (K=128);
  * 5 FP8 with A in tensor memory (K=128); 6 mode 0 followed by mode 3 into the
- * same accumulator.  a: [128][K] row-major (bytes per element as the mode's
- * type; for mode 6, a holds the 128x128 FP8 A then the 128x16 BF16 A), b:
- * [N][K] row-major likewise, d: fp32 [128][N]; N = 128. */
+ * same accumulator; 7 NVFP4 block-scaled (K=128, 64-byte swizzle, scale
+ * factors copied to tensor memory).  a: [128][K] row-major (bytes per element
+ * as the mode's type; for mode 6, a holds the 128x128 FP8 A then the 128x16
+ * BF16 A; for mode 7, [128][64] packed E2M1 bytes, element 2i in the low
+ * nibble, then [128][8] UE4M3 scales, one per 16 elements along K), b: [N][K]
+ * row-major likewise, d: fp32 [128][N]; N = 128. */
 int vca_debug_mma(int mode, const void* a, const void* b, float* d, vca_stream_t stream);
 
 #ifdef __cplusplus

@@ -47,7 +47,7 @@ def test_state_bytes_and_layout(L):
     assert all(o % 1024 == 0 for o, _ in offs)
     assert offs[-1][0] < a.total_bytes
     c = vca.state_layout(1, 2, 700, 128, 8, 4)
-    assert c.q4 and c.r4s and not c.qhat
+    assert c.q4 and c.kr4s and not c.qhat
 
 
 def test_prepare_rejects_bad_arguments(L):

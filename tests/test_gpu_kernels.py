@@ -112,3 +112,33 @@ def test_mma_mixed_kinds_one_accumulator(V):
     got = _run_mma(V, 6, ta, tb)
     ref = A8.astype(np.float64) @ B8.T + A16.astype(np.float64) @ B16.T
     assert np.array_equal(got, ref)
+
+
+def _nvfp4_operand(rng, pow2_scales):
+    """[128][64] packed E2M1 bytes (element 2i in the low nibble) followed by
+    [128][8] UE4M3 scales; returns the bytes and the decoded [128][128] matrix."""
+    from oracle import e2m1_decode, e4m3_decode
+    codes = rng.integers(0, 16, (128, 128)).astype(np.uint8)
+    if pow2_scales:
+        sc = np.array([0x28, 0x30, 0x38, 0x40, 0x48], np.uint8)[rng.integers(0, 5, (128, 8))]
+    else:
+        sc = rng.integers(0x20, 0x50, (128, 8)).astype(np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    val = e2m1_decode(codes).reshape(128, 128) * np.repeat(e4m3_decode(sc).reshape(128, 8), 16, 1)
+    raw = np.concatenate([packed.ravel(), sc.ravel()])
+    return torch.from_numpy(raw), val
+
+
+@pytest.mark.parametrize("pow2_scales", [True, False])
+def test_mma_nvfp4_block_scaled(V, pow2_scales):
+    """kind::mxf4nvf4 with UE4M3 scales per 16 elements: the product of the
+    decoded operands.  With power-of-two scales every partial sum is exact in
+    fp32; with general scales the tensor core may round its partial sums."""
+    rng = np.random.default_rng(70 + pow2_scales)
+    ta, A = _nvfp4_operand(rng, pow2_scales)
+    tb, Bm = _nvfp4_operand(rng, pow2_scales)
+    got = _run_mma(V, 7, ta, tb)
+    ref = A @ Bm.T
+    tol = (1e-6 if pow2_scales else 1e-5) * np.abs(ref).max()
+    err = np.abs(got - ref)
+    assert err.max() <= tol, f"max |err| {err.max()} (tol {tol}), {np.sum(err > tol)} mismatches"
