@@ -32,8 +32,11 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "attention TFLOPS & % of GB300 FP8 tensor peak at N=75600,H=40,d=128; V-Smooth ms"
-FP8_NOMINAL_TFLOPS = 4500.0   # dense FP8 per GPU (NVIDIA nominal)
-FP8_PER_BF16 = 2.0            # nominal FP8 : BF16 dense ratio
+# Dense tensor peaks per GPU (NVIDIA nominal) and their nominal ratio to BF16,
+# by the bit width of the attention operands: FP8 (8) and FP4 (4).
+NOMINAL_TFLOPS = {8: 4500.0, 4: 13500.0}
+PER_BF16 = {8: 2.0, 4: 6.0}
+PEAK_NAME = {8: "fp8", 4: "fp4"}
 
 # DRAM bytes (read + write) of one FP8 attention launch, from one ncu capture
 # of the sweep16k workload (B1 H24 N16384): 154.6 MB read + 70.0 MB written.
@@ -64,20 +67,24 @@ def attn_traffic(w):
             if hashlib.sha256(f.read()).hexdigest() != digest:
                 return None
     if w.bits != 8:
-        return None
+        return None     # the 4-bit kernel has no capture yet
     return ATTN_TRAFFIC["bytes"] * (w.B * w.H * w.N) / ATTN_TRAFFIC["tokens"]
 
 
 def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
-    """Algorithmic DRAM bytes of one V-Smooth preparation (8-bit): read Q, K,
-    V (bf16) once for the quantisers and V once more for the grouping
-    features; write the int8 features, read them once per Lloyd iteration;
-    write the E4M3 codes of Q, K and R^T, the permutation, the block means
-    (bf16 and fp32) and the per-block scales."""
+    """Algorithmic DRAM bytes of one V-Smooth preparation: read Q, K, V (bf16)
+    once for the quantisers and V once more for the grouping features; write
+    the int8 features, read them once per Lloyd iteration; write the codes of
+    Q, K and R^T (E4M3, or E2M1 plus one UE4M3 scale per 16), the
+    permutation, the block means and the scales."""
     BH, N, d = w.B * w.H, w.N, w.d
     nb = (N + 127) // 128
     npad = nb * 128
-    total = 3 * BH * N * d * 2 + 3 * BH * npad * d + BH * nb * d * (2 + 4) + BH * nb * 8
+    total = 3 * BH * N * d * 2
+    if w.bits == 8:
+        total += 3 * BH * npad * d + BH * nb * d * (2 + 4) + BH * nb * 8
+    else:
+        total += 3 * BH * npad * d * (1 / 2 + 1 / 16) + BH * nb * d * 2
     total += 4 * BH * N * 2                     # permutation: written, read by the gathers
     if not reuse:
         total += BH * N * d * 2                 # V read by the feature pass
@@ -86,12 +93,14 @@ def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
     return float(total)
 
 
-def launches_per_step(iters: int, reuse: bool) -> int:
+def launches_per_step(iters: int, reuse: bool, bits: int = 8) -> int:
     """Kernels of libvca launched by one step (preparation chain + attention)."""
     grouping = 0 if reuse else (1 + 1 + 1 + 1 + 2 * iters + 3)  # zero, amax, features, init, iters, sort
-    # header, grouping, Q/K/V passes (Q, K sums, K mean, K, V1, V reduce, zero, V2),
-    # header-done, attention
-    return 1 + grouping + 8 + 1 + 1
+    # 8-bit Q/K/V passes: Q, K, V1, V reduce, zero, V2; 4-bit: zero, |Q| max,
+    # |K'| max, V1, global scales, Q, K, zero, V2
+    passes = 6 if bits == 8 else 9
+    # header, grouping, key sums + key mean, the passes, header-done, attention
+    return 1 + grouping + 2 + passes + 1 + 1
 
 
 class ClockSampler:
@@ -150,11 +159,13 @@ def cpu_oracle_sample(w, rows_per_head=16, seed_rows=0):
     oracle.build()
     q, k, v = synth.make_qkv(1, 1, w.N, w.d, w.clusters, w.seed)
     t0 = time.perf_counter()
-    p = oracle.prepare8(q[0, 0], k[0, 0], v[0, 0], w.k, 10, 0, b=0, h=0, H=1)
+    prepare, attention = ((oracle.prepare8, oracle.attention8) if w.bits == 8
+                          else (oracle.prepare4, oracle.attention4))
+    p = prepare(q[0, 0], k[0, 0], v[0, 0], w.k, 10, 0, b=0, h=0, H=1)
     t_prep = time.perf_counter() - t0
     rows = np.random.default_rng(seed_rows).choice(w.N, rows_per_head, replace=False)
     t0 = time.perf_counter()
-    oracle.attention8(p, rows)
+    attention(p, rows)
     t_rows = time.perf_counter() - t0
     heads = w.B * w.H
     t_step = heads * (t_prep + t_rows * w.N / rows_per_head)
@@ -287,7 +298,8 @@ def run_gpu(args, w):
     attn_avg = statistics.mean(attn_ms)
     attn_tflops = w.flops / (attn_avg * 1e-3) / 1e12
     pk = peaks()
-    fp8_peak = pk["bf16_sus"] * FP8_PER_BF16
+    tc_peak = pk["bf16_sus"] * PER_BF16[w.bits]
+    pname = PEAK_NAME[w.bits]
 
     # end to end through the public API: pinned H2D of Q, K, V, prepare,
     # attention, D2H of O, every step
@@ -331,23 +343,23 @@ def run_gpu(args, w):
                    "l2": "inputs (3 x %.2f GB) larger than L2; no flush" % (nbytes / 1e9),
                    "parallelism": f"independent problem per GPU x{world}"},
         "attention_ms": attn_avg, "attention_tflops": attn_tflops,
-        "pct_fp8_peak": 100.0 * attn_tflops / fp8_peak,
-        "pct_fp8_nominal": 100.0 * attn_tflops / FP8_NOMINAL_TFLOPS,
+        f"pct_{pname}_peak": 100.0 * attn_tflops / tc_peak,
+        f"pct_{pname}_nominal": 100.0 * attn_tflops / NOMINAL_TFLOPS[w.bits],
         "vsmooth_ms": statistics.mean(prep_ms),
         "vsmooth_gbs": vsmooth_bytes(w, args.iters, args.reuse) / (statistics.mean(prep_ms) * 1e-3)
         / 1e9,
         "vsmooth_bytes": vsmooth_bytes(w, args.iters, args.reuse),
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": attn_tflops / fp8_peak, "traffic": attn_traffic(w),
-                     "kernel": "attn_fp8_kernel",
-                     "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x {FP8_PER_BF16} "
-                                 "(nominal FP8:BF16 ratio)"},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "traffic": attn_traffic(w),
+                     "kernel": "attn_fp8_kernel" if w.bits == 8 else "attn_nvfp4_kernel",
+                     "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
+                                 f"{PER_BF16[w.bits]} (nominal {pname.upper()}:BF16 ratio)"},
         "e2e": ({"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                  "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * nbytes,
                  "d2h_bytes_per_step": nbytes} if e2e_ms else None),
-        "gpu_launches": launches_per_step(args.iters, args.reuse) * args.steps,
+        "gpu_launches": launches_per_step(args.iters, args.reuse, w.bits) * args.steps,
         "clocks": clocks.summary(),
     }
     if dist:

@@ -1,7 +1,7 @@
 """GPU: the full Wan2.2-like 720p workload (B=1, H=40, N=75600, k=64, 10
-iterations) in the launch configuration the benchmark times; preparation of
-two sampled heads is bit-exact with the oracle and sampled attention rows are
-within relative L2 2e-3."""
+iterations) in the launch configuration the benchmark times, at 8 and 4 bits;
+preparation of two sampled heads is bit-exact with the oracle and sampled
+attention rows are within relative L2 2e-3 (8-bit) and 1e-2 (4-bit)."""
 import numpy as np
 import pytest
 import torch
@@ -38,3 +38,29 @@ def test_wan720p_sampled_parity(orc):
         err = rel_l2(got, ref)
         print(f"head {h}: relative L2 vs oracle {err:.2e}")
         assert err <= 2e-3
+
+
+def test_wan720p_nvfp4_sampled_parity(orc):
+    from bit_attention_video_gb300 import vca
+    from test_gpu_nvfp4 import check_head4
+    w = synth.CONFIGS["wan720p_fp4"]
+    shape = (w.B, w.H, w.N, w.d)
+    host = [torch.empty(shape, dtype=torch.bfloat16) for _ in range(3)]
+    q, k, v = synth.make_qkv(w.B, w.H, w.N, w.d, w.clusters, w.seed,
+                             out=tuple(h.view(torch.int16).numpy().view(np.uint16) for h in host))
+    dq, dk, dv = (h.cuda() for h in host)
+    att = vca.VCAttention(*shape, k_clusters=w.k, bits=4, iters=10, seed=0)
+    out = att(dq, dk, dv)
+    assert att.status() == 0
+    views = {n: t.cpu().numpy() for n, t in vca.state_view(att.state, shape, w.k, 4).items()}
+    rng = np.random.default_rng(21)
+    for h in (1, w.H - 2):
+        p = orc.prepare4(q[0, h], k[0, h], v[0, h], w.k, 10, 0, b=0, h=h, H=w.H)
+        check_head4(views, p, h, w.N, what=("labels", "perm"))
+        rows = np.sort(np.concatenate([rng.choice(w.N - 128, 24, replace=False),
+                                       np.arange(w.N - 8, w.N)]))
+        _, ref = orc.attention4(p, rows)
+        got = bf16_f64(to_np_u16(out[0, h][torch.from_numpy(rows).cuda()]))
+        err = rel_l2(got, ref)
+        print(f"head {h}: 4-bit relative L2 vs oracle {err:.2e}")
+        assert err <= 1e-2
