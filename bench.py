@@ -200,6 +200,21 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, dist, device) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's own problem over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def time_e2e(e2e_step, args, stream, dist, dev):
     import torch
     e2e_step()
@@ -213,12 +228,7 @@ def time_e2e(e2e_step, args, stream, dist, dev):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return ms
+    return max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
 
 def run_gpu(args, w):
@@ -282,11 +292,7 @@ def run_gpu(args, w):
             step(evs[i])
         t1.record(stream)
         torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     st = att.status()
@@ -294,7 +300,7 @@ def run_gpu(args, w):
         raise RuntimeError(f"device status {st} after the timed steps")
 
     ms_per_step = total_ms / args.steps
-    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    value = weak_value(world, w.flops, ms_per_step)
     attn_avg = statistics.mean(attn_ms)
     attn_tflops = w.flops / (attn_avg * 1e-3) / 1e12
     pk = peaks()
@@ -356,7 +362,7 @@ def run_gpu(args, w):
                      "kernel": "attn_fp8_kernel" if w.bits == 8 else "attn_nvfp4_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
                                  f"{PER_BF16[w.bits]} (nominal {pname.upper()}:BF16 ratio)"},
-        "e2e": ({"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        "e2e": ({"value": weak_value(world, w.flops, e2e_ms), "unit": "TFLOPS",
                  "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * nbytes,
                  "d2h_bytes_per_step": nbytes} if e2e_ms else None),
         "gpu_launches": launches_per_step(args.iters, args.reuse, w.bits) * args.steps,
