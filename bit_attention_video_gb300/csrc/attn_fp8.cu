@@ -1,27 +1,33 @@
 // 8-bit VC-Attention forward (paper §3.1 Eq 1, §3.2 Eq 6, §3.3 Eq 7) on
 // tcgen05 tensor cores.
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams all
-// key blocks j of the permuted, centred keys K' and the transposed residual
-// R^T through a TMA ring.  Warp roles:
-//   warp 0        producer: TMA of the Q tile once; per stage K'_j, R^T_j and
-//                 the 16 "slot" rows appended to R^T_j (written by the warp's
-//                 lanes); the mean operand of each group of 8 blocks
+// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and
+// streams all key blocks j of the permuted, centred keys K' and the
+// transposed residual R^T through a TMA ring; both tiles consume each stage.
+// Warp roles (12 warps):
+//   warp 0        producer: TMA of the two Q tiles once; per stage K'_j, R^T_j
+//                 and the 16 "slot" rows appended to R^T_j (written by the
+//                 warp's lanes); the mean operand of each group of 8 blocks
 //   warp 1        MMA issuer (warp-uniform loop, one elected lane issues;
 //                 busy-polling) and TMEM owner
-//   warps 4-11    softmax + correction + epilogue: two threads per query row
-//                 (key columns 0-63 and 64-127, output columns 0-63 and
-//                 64-127), which exchange the partial row maximum
+//   warps 4-7     softmax + correction + epilogue of tile A, warps 8-11 of
+//                 tile B: one thread per query row, which holds the row's 128
+//                 scores in registers (so each SM sub-partition carries one
+//                 softmax warp per tile beside the MMA or producer warp)
 //
-// Tensor memory (448 of 512 columns):
-//   [0,128), [128,256)  S_j = Q^ K'_j^T in buffer j % 2 (fp32)
-//   [256,384)  the output accumulator A (128 channels)
-//   [384,400)  two banks of 8 row-sum slots (see below), part of the same
-//              accumulator, so the alpha rescaling covers them
-//   [400,432)  P^_j (ExpCast bytes, 4 per column), the A operand of the product
-//   [432,448)  a group's row-sum operand (bf16 hi, lo) of the mean product
+// Tensor memory (512 columns):
+//   [0,128)    S = Q^ K'^T (fp32), one buffer shared by the two tiles: the
+//              softmax releases it as soon as it has loaded its scores
+//   per tile X at base 128 + 192 X:
+//     [+0,+128)    the output accumulator A_X
+//     [+128,+144)  two banks of 8 row-sum slots, part of the same accumulator
+//     [+144,+176)  P^_X (ExpCast bytes, 4 per column): A operand of the product
+//     [+176,+192)  a group's row-sum operand (bf16 hi, lo) of the mean product
+// The MMA warp issues S_A(j+1) before PV_A(j) (P has its own columns), so a
+// tile's next scores are ready when its softmax finishes a block, and the two
+// tiles' softmaxes run concurrently, each handing the S buffer to the other.
 //
-// Per key block j:
+// Per key block j and tile:
 //   S   = Q^ K'^_j^T                              FP8 MMA (N=128)
 //   M'  = max(M, a_j rowmax(S))                   exact running max (x8, log2)
 //   c   = clip_[0,120](RNE(a_j S + 119.65 - M'))  ExpCast-FP8 bytes -> TMEM
@@ -29,12 +35,13 @@
 //   A  += P^ [R^_j ; E_j]                          FP8 MMA (N=144), A from TMEM
 // E_j (16 rows of K=128) is zero except row 8*bank + slot of block j, which is
 // all ones: column 128 + 8 bank + slot of the product is the row sum r_j of
-// exactly the bytes the product consumes.  Blocks form groups of 8 (aligned
-// to the last block; only the first group can be partial) that alternate
-// between the two banks.  After a group's last product the softmax reads its
-// 8 slots rho (rescaled like the accumulator), adds them to l, clears the bank
-// and writes rho as bf16 hi/lo to TMEM; three BF16 K=16 MMAs then add
-// sum_g rho_g mutilde_g^T (Eq 6's mean term, hi/lo split of both factors).
+// exactly the bytes the product consumes, at the maximum M_j of block j.
+// Blocks form groups of 8 (aligned to the last block; only the first group can
+// be partial) that alternate between the two banks; the correction rescales
+// the banks with the accumulator.  After a group's last product the softmax
+// reads its 8 slots (already at the current maximum), adds them to l, clears
+// the bank and writes the slots as bf16 hi/lo to TMEM; three BF16 K=16 MMAs
+// then add sum_g rho_g mutilde_g^T (Eq 6's mean term).
 // Epilogue: O = sV (.) A / l in bf16, original query order (Q is not permuted).
 #include "common.cuh"
 #include "expcast.cuh"
@@ -46,12 +53,11 @@ namespace {
 constexpr int kStages = 5;
 constexpr uint32_t kSlotRowsBytes = 16 * 128;                      // E_j: 16 rows x 128 keys
 constexpr uint32_t kStageBytes = 2 * kTileBytes + kSlotRowsBytes;  // K'_j, R^T_j, E_j
-constexpr uint32_t OFF_Q = 0;                                      // the query tile
-constexpr uint32_t OFF_KV = kTileBytes;
+constexpr uint32_t OFF_Q = 0;                                      // the two query tiles
+constexpr uint32_t OFF_KV = 2 * kTileBytes;
 constexpr uint32_t OFF_BG = OFF_KV + kStages * kStageBytes;    // mean operand, 2 buffers x 8 KB
 constexpr uint32_t OFF_SV = OFF_BG + 2 * kGroupBytes;          // sV, 512 B
-constexpr uint32_t OFF_XCH = OFF_SV + 512;                     // partial row max, 2 x 2 x 128 x 4 B
-constexpr uint32_t OFF_BAR = OFF_XCH + 2048;
+constexpr uint32_t OFF_BAR = OFF_SV + 512;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
 constexpr int kThreads = 384;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -59,7 +65,11 @@ static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 static_assert(kGroup == 8, "eight row-sum slots per bank");
 
 // TMEM columns
-constexpr uint32_t TC_S = 0, TC_ACC = 256, TC_BANK = 384, TC_P = 400, TC_GHI = 432, TC_GLO = 440;
+constexpr uint32_t TC_S = 0;
+__device__ __forceinline__ uint32_t tc_acc(int X) { return 128u + 192u * X; }
+__device__ __forceinline__ uint32_t tc_p(int X) { return tc_acc(X) + 144u; }
+__device__ __forceinline__ uint32_t tc_ghi(int X) { return tc_acc(X) + 176u; }
+__device__ __forceinline__ uint32_t tc_glo(int X) { return tc_acc(X) + 184u; }
 
 struct Fp8Params {
   const float* sq;        // [BH][nb]
@@ -69,14 +79,14 @@ struct Fp8Params {
   const uint32_t* hdr;
   uint16_t* out;          // [BH][N][128]
   int* status;
-  int B, H, N, nb, Npad, ngroups, gpad;
+  int B, H, N, nb, Npad, ngroups, gpad, npairs;
   float qk_scale;         // 8 log2(e) / sqrt(128)
 };
 
-// barrier indices
+// barrier indices ([2]: per tile)
 enum { B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = B_KVFULL + kStages, B_SFULL = B_KVEMPTY + kStages,
-       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 1,
-       B_DRAIN = B_PVDONE + 1, B_COUNT = B_DRAIN + 1 };
+       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2,
+       B_DRAIN = B_PVDONE + 2, B_COUNT = B_DRAIN + 1 };
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -95,6 +105,15 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -125,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nb = p.nb, gpad = p.gpad;
-  const int bh = blockIdx.x / nb, qt = blockIdx.x % nb;
+  const int bh = blockIdx.x / p.npairs, qp = blockIdx.x % p.npairs;
+  const bool has_b = 2 * qp + 1 < nb;   // the last pair of an odd nb has tile A only
 
   // Skip the launch if the blob is in an error state or not an 8-bit
   // preparation of this shape (uniform over the CTA).
@@ -141,10 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (threadIdx.x == 0) {
-    // producer/MMA barriers complete on one arrival (or a tcgen05 commit);
-    // "S read" and "P written" complete when all 256 softmax threads arrive
+    // "S read" and "P written": the 128 softmax threads of a tile; the
+    // rest: one arrival or a tcgen05 commit
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 256 : 1);
+      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 128 : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmQ);
@@ -166,13 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     bool ok = true;
     if (lane == 0) {
-      mbar_expect_tx(bar(B_QFULL), kTileBytes);
-      tma_load_2d(base + OFF_Q, &tmQ, bar(B_QFULL), 0, bh * p.Npad + qt * 128);
+      mbar_expect_tx(bar(B_QFULL), (has_b ? 2 : 1) * kTileBytes);
+      tma_load_2d(base + OFF_Q, &tmQ, bar(B_QFULL), 0, bh * p.Npad + 2 * qp * 128);
+      if (has_b)
+        tma_load_2d(base + OFF_Q + kTileBytes, &tmQ, bar(B_QFULL), 0, bh * p.Npad + (2 * qp + 1) * 128);
     }
     int issued = 0;
     for (int j = 0; j < nb; ++j) {
       const int s = j % kStages;
-      if (j >= kStages) ok = mbar_wait(bar(B_KVEMPTY + s), ((j / kStages) - 1) & 1, abort_flag, p.status);
+      if (j >= kStages)
+        ok = mbar_wait(bar(B_KVEMPTY + s), ((j / kStages) - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint32_t st = base + OFF_KV + s * kStageBytes;
       // E_j: 16 rows of 128 bytes (a 128-byte-swizzled tile whose rows are
@@ -215,168 +238,176 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (uniform control flow, operands in
     // uniform registers); one elected lane issues each MMA and commit.
-    // S_0, S_1 up front; per block j, once P^_j is in TMEM: P^ [R^_j; E_j],
-    // the mean product of a group closed by block j-1, and S_{j+2} into the
-    // buffer the softmax released after reading S_j.
-    {
-      const uint32_t i8 = idesc_f8(128, 128), i8w = idesc_f8(128, 144),
-                     i16 = idesc_bf16(128, 128);
-      const uint64_t dq = desc_k_sw128(base + OFF_Q);
-      const uint64_t dk0 = desc_k_sw128(base + OFF_KV);                  // stage 0 K'
-      const uint64_t dr0 = desc_k_sw128(base + OFF_KV + kTileBytes);     // stage 0 [R^; E]
-      const uint64_t dstage = kStageBytes >> 4;                          // per-stage step
-      const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256);
-      const uint64_t dgroup = kGroupBytes >> 4, dhalf = (kGroupBytes / 2) >> 4;
-      bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, p.status);
-      auto issue_s = [&](int j) {
-        const int s = j % kStages;
-        ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
-        tc_fence_after();
-        const uint64_t dk = dk0 + s * dstage;
-        const uint32_t d = tmem + TC_S + 128 * (j & 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_f8_ss_w(d, dq + 2 * kk, dk + 2 * kk, i8, kk > 0);
-        mma_commit_w(bar(B_SFULL + (j & 1)));
-      };
-      auto issue_flush = [&](int g) {
+    // Order: S_A(0), S_B(0); per block j: S_A(j+1), PV_A(j), S_B(j+1), PV_B(j)
+    // (each S waits for the other tile to have loaded the shared S buffer).
+    const uint32_t i8 = idesc_f8(128, 128), i8w = idesc_f8(128, 144), i16 = idesc_bf16(128, 128);
+    const uint64_t dq0 = desc_k_sw128(base + OFF_Q);
+    const uint64_t dqstep = kTileBytes >> 4;
+    const uint64_t dk0 = desc_k_sw128(base + OFF_KV);                  // stage 0 K'
+    const uint64_t dr0 = desc_k_sw128(base + OFF_KV + kTileBytes);     // stage 0 [R^; E]
+    const uint64_t dstage = kStageBytes >> 4;                          // per-stage step
+    const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256);
+    const uint64_t dgroup = kGroupBytes >> 4, dhalf = (kGroupBytes / 2) >> 4;
+    bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, p.status);
+    auto issue_s = [&](int X, int j) {
+      const int s = j % kStages;
+      ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+      tc_fence_after();
+      const uint64_t dk = dk0 + s * dstage, dq = dq0 + X * dqstep;
+      mma4_f8_ss_w(tmem + TC_S, dq, dk, i8, 0);
+      mma_commit_w(bar(B_SFULL + X));
+    };
+    auto issue_pv = [&](int X, int j) {
+      ok = mbar_wait_spin(bar(B_PFULL + X), j & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+      tc_fence_after();
+      const uint64_t dr = dr0 + (j % kStages) * dstage;
+      mma4_f8_ts_w(tmem + tc_acc(X), tmem + tc_p(X), dr, i8w, j > 0);
+      if (j > 0 && group_ends(j - 1, nb, gpad)) {
         // sum_g rho_g mutilde_g^T = rho_hi mu_hi + rho_lo mu_hi + rho_hi mu_lo
-        const uint64_t bg = dbg0 + (g & 1) * dgroup;
-        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GHI, bg, i16, 1);
-        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GLO, bg, i16, 1);
-        mma_f16_ts_w(tmem + TC_ACC, tmem + TC_GHI, bg + dhalf, i16, 1);
-      };
+        const uint64_t bg = dbg0 + (((j - 1 + gpad) / kGroup) & 1) * dgroup;
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg, i16, 1);
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_glo(X), bg, i16, 1);
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg + dhalf, i16, 1);
+      }
+      mma_commit_w(bar(B_PVDONE + X));
+    };
+    auto wait_sfree = [&](int X, int j) {
+      ok = mbar_wait_spin(bar(B_SFREE + X), j & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
-      for (int j = 0; ok && j < min(2, nb); ++j) issue_s(j);
-      for (int j = 0; ok && j < nb; ++j) {
-        ok = mbar_wait_spin(bar(B_PFULL), j & 1, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t dr = dr0 + (j % kStages) * dstage;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8_ts_w(tmem + TC_ACC, tmem + TC_P + 8 * kk, dr + 2 * kk, i8w, (j > 0 || kk > 0));
-        if (j > 0 && group_ends(j - 1, nb, gpad)) issue_flush((j - 1 + gpad) / kGroup);
-        mma_commit_w(bar(B_PVDONE));
-        mma_commit_w(bar(B_KVEMPTY + j % kStages));
-        if (j + 2 < nb) {
-          ok = mbar_wait_spin(bar(B_SFREE + (j & 1)), (j >> 1) & 1, abort_flag, p.status);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          issue_s(j + 2);
-        }
-      }
-      // the last group's mean product, after the softmax read its row sums
-      if (ok) {
-        ok = mbar_wait_spin(bar(B_PFULL), nb & 1, abort_flag, p.status);
-        if (__all_sync(0xffffffffu, ok)) {
-          tc_fence_after();
-          issue_flush((nb - 1 + gpad) / kGroup);
-          mma_commit_w(bar(B_PVDONE));
-        }
-      }
-      // all issued MMAs complete before the CTA releases its tensor memory
-      mma_commit_w(bar(B_DRAIN));
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
-      }
+    };
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) issue_s(0, 0);
+    if (ok && has_b) {
+      wait_sfree(0, 0);
+      if (ok) issue_s(1, 0);
     }
-  } else if (warp >= 4) {
+    for (int j = 0; ok && j < nb; ++j) {
+      if (j + 1 < nb) {
+        wait_sfree(has_b ? 1 : 0, j);   // the other tile (or tile A itself) loaded block j
+        if (!ok) break;
+        issue_s(0, j + 1);
+        if (!ok) break;
+      }
+      issue_pv(0, j);
+      if (!ok) break;
+      if (has_b) {
+        if (j + 1 < nb) {
+          wait_sfree(0, j + 1);
+          if (!ok) break;
+          issue_s(1, j + 1);
+          if (!ok) break;
+        }
+        issue_pv(1, j);
+        if (!ok) break;
+      }
+      mma_commit_w(bar(B_KVEMPTY + j % kStages));
+    }
+    // the last group's mean product, after the softmax read its row sums
+    for (int X = 0; ok && X < (has_b ? 2 : 1); ++X) {
+      ok = mbar_wait_spin(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t bg = dbg0 + (((nb - 1 + gpad) / kGroup) & 1) * dgroup;
+      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg, i16, 1);
+      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_glo(X), bg, i16, 1);
+      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg + dhalf, i16, 1);
+      mma_commit_w(bar(B_PVDONE + X));
+    }
+    // all issued MMAs complete before the CTA releases its tensor memory
+    mma_commit_w(bar(B_DRAIN));
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+    }
+  } else if (warp >= 4 && (warp < 8 || has_b)) {
     // ------------------------------------------------------------ softmax
-    const int h = (warp - 4) / 4, quarter = warp % 4;
+    const int X = (warp - 4) / 4, quarter = warp % 4;
+    const int qt = 2 * qp + X;
     const int row = quarter * 32 + lane;  // row within the query tile = TMEM lane
-    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tl = tmem + lanes;
-    const uint32_t named = 1 + quarter;   // barrier of the two warps sharing these rows
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t acc = tl + tc_acc(X);
     const float a_q = p.qk_scale * p.sq[(size_t)bh * nb + qt];
     const float* skp = p.sk + (size_t)bh * nb;
-    const int valid_last = p.N - (nb - 1) * 128 - 64 * h;  // valid columns of this half, last block
-    // [block parity][h][row]: the slot written in block j is not rewritten
-    // before the partner has passed the barrier of block j + 1
-    float* xch_base = reinterpret_cast<float*>(sm + OFF_XCH);
+    const int valid_last = p.N - (nb - 1) * 128;  // valid keys of the last block
     float M = -INFINITY, l = 0.0f;
     float sk_next = __ldg(skp);
     bool ok = true;
-    // After group g's last product: read its 8 row-sum slots (already rescaled
-    // to the current maximum), add them to l, clear the bank (half 0) and
-    // write the bf16 operand (half 0: hi, half 1: lo; slots 2c, 2c+1 in column
-    // c, columns 4-7 = K 8..15 = 0).
+    // After group g's last product: read its 8 row-sum slots (already at the
+    // current maximum), add them to l, clear the bank and write the bf16
+    // operand (hi in the first 8 columns, lo in the next 8; slots 2c, 2c+1 in
+    // column c, columns 4-7 = K 8..15 = 0).
     auto close_group = [&](int g) {
-      const uint32_t bank = tl + TC_BANK + 8 * (g & 1);
+      const uint32_t bank = acc + 128 + 8 * (g & 1);
       uint32_t v[8];
       tmem_ld8(bank, v);
       tmem_ld_wait();
       float rsum = 0.0f;
-      uint32_t pk[8];
+      uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float r0 = __uint_as_float(v[2 * c]), r1 = __uint_as_float(v[2 * c + 1]);
         rsum += r0 + r1;
-        uint16_t h0 = f32_to_bf16_bits(r0), h1 = f32_to_bf16_bits(r1);
-        if (h) {
-          h0 = f32_to_bf16_bits(r0 - bf16_bits_to_f32(h0));
-          h1 = f32_to_bf16_bits(r1 - bf16_bits_to_f32(h1));
-        }
+        const uint16_t h0 = f32_to_bf16_bits(r0), h1 = f32_to_bf16_bits(r1);
+        const uint16_t l0 = f32_to_bf16_bits(r0 - bf16_bits_to_f32(h0));
+        const uint16_t l1 = f32_to_bf16_bits(r1 - bf16_bits_to_f32(h1));
         pk[c] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        pk[8 + c] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+        pk[4 + c] = 0u;
+        pk[12 + c] = 0u;
       }
-#pragma unroll
-      for (int c = 4; c < 8; ++c) pk[c] = 0u;
       l += rsum;
-      tmem_st8(tl + (h ? TC_GLO : TC_GHI), pk);
-      // both halves have read the bank before half 0 clears it
-      asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
-      if (h == 0) {
-        uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        tmem_st8(bank, z);
-      }
+      tmem_st16(tl + tc_ghi(X), pk);
+      uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      tmem_st8(bank, z);
     };
     for (int j = 0; j < nb; ++j) {
-      const uint32_t sbuf = tl + TC_S + 128 * (j & 1);
       const float a = a_q * sk_next;
       if (j + 1 < nb) sk_next = __ldg(skp + j + 1);
-      ok = mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_SFULL + X), j & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t s[64];
-      tmem_ld32(sbuf + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(sbuf + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      // all 128 scores of the row into registers, then release the S buffer
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tl + TC_S + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_SFREE + (j & 1)));
-      if (j == nb - 1 && valid_last < 64) {
+      mbar_arrive(bar(B_SFREE + X));
+      if (j == nb - 1 && valid_last < 128) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 128; ++c)
           if (c >= valid_last) s[c] = 0xFF800000u;  // -inf: masked key -> byte 0
       }
-      // partial row maximum (four chains), exchanged with the partner thread
-      float m4[4];
+      // row maximum (eight chains of three-input max)
+      float m8[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m4[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
-      for (int c = 8; c < 64; c += 8)
+      for (int c = 16; c < 128; c += 16)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          m4[i] = max3(m4[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-      float* xch = xch_base + (j & 1) * 256;
-      xch[h * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
-      const float mx = fmaxf(xch[row], xch[128 + row]);
+        for (int i = 0; i < 8; ++i)
+          m8[i] = max3(m8[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+      const float mx = fmaxf(fmaxf(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5])),
+                             fmaxf(m8[6], m8[7]));
       const float Mn = fmaxf(M, a * mx);
       const float alpha = ex2((M - Mn) * 0.125f);  // 0 on the first block
       const float b = kExpCastBias - Mn;
-      // this half's ExpCast bytes, four per 32-bit TMEM column (the A layout of
-      // the product: byte k of column c is key 4c + k)
-      uint32_t w[16];
+      // ExpCast bytes, four per 32-bit TMEM column (the A layout of the
+      // product: byte k of column c is key 4c + k)
+      uint32_t w[32];
       if (expcast_fast_is_exact(Mn)) {
         const float a128 = a * 0.0078125f, b128 = b * 0.0078125f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < 128; c += 4) {
           const uint2 e0 = expcast_pair_bits(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), a128, b128);
           const uint2 e1 = expcast_pair_bits(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), a128, b128);
           w[c / 4] = __byte_perm(__byte_perm(e0.x, e0.y, 0x0040), __byte_perm(e1.x, e1.y, 0x0040), 0x5410);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; c += 4)
+        for (int c = 0; c < 128; c += 4)
           w[c / 4] = expcast_code(__uint_as_float(s[c]), a, b) |
                      (expcast_code(__uint_as_float(s[c + 1]), a, b) << 8) |
                      (expcast_code(__uint_as_float(s[c + 2]), a, b) << 16) |
@@ -384,33 +415,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j > 0) {
         // the previous product read P^ and wrote the accumulator
-        ok = mbar_wait(bar(B_PVDONE), (j - 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(bar(B_PVDONE + X), (j - 1) & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
-      tmem_st16(tl + TC_P + 16 * h, w);
+      tmem_st16(tl + tc_p(X), *reinterpret_cast<uint32_t(*)[16]>(&w[0]));
+      tmem_st16(tl + tc_p(X) + 16, *reinterpret_cast<uint32_t(*)[16]>(&w[16]));
       if (j > 0) {
-        // correction: rescale this half of the accumulator row and this half's
-        // row-sum bank when the running max rose
+        // correction: rescale the accumulator row and both row-sum banks
+        // when the running max rose
         if (__any_sync(0xffffffffu, alpha < 1.0f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
+          for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tl + TC_ACC + 64 * h + c0, v);
+            tmem_ld32(acc + c0, v);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-            tmem_st32(tl + TC_ACC + 64 * h + c0, v);
+            tmem_st32(acc + c0, v);
           }
-          uint32_t v8[8];
-          tmem_ld8(tl + TC_BANK + 8 * h, v8);
+          uint32_t v16[16];
+          tmem_ld16(acc + 128, v16);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) v8[c] = __float_as_uint(__uint_as_float(v8[c]) * alpha);
-          tmem_st8(tl + TC_BANK + 8 * h, v8);
-          tmem_st_wait();
-          // both halves must finish rescaling before either reads a bank
-          asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
+          for (int c = 0; c < 16; ++c) v16[c] = __float_as_uint(__uint_as_float(v16[c]) * alpha);
+          tmem_st16(acc + 128, v16);
         }
         l *= alpha;
         if (group_ends(j - 1, nb, gpad)) close_group((j - 1 + gpad) / kGroup);
@@ -418,18 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       M = Mn;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + X));
     }
     if (ok) {
       // the last group's row sums and mean product
-      ok = mbar_wait(bar(B_PVDONE), (nb - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_PVDONE + X), (nb - 1) & 1, abort_flag, p.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         close_group((nb - 1 + gpad) / kGroup);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
-        ok = mbar_wait(bar(B_PVDONE), nb & 1, abort_flag, p.status);
+        mbar_arrive(bar(B_PFULL + X));
+        ok = mbar_wait(bar(B_PVDONE + X), nb & 1, abort_flag, p.status);
       } else {
         ok = false;
       }
@@ -438,12 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int grow = qt * 128 + row;
       const float inv_l = 1.0f / l;
-      uint16_t* orow = p.out + ((size_t)bh * p.N + grow) * 128 + 64 * h;
-      const float* svh = s_sv + 64 * h;
+      uint16_t* orow = p.out + ((size_t)bh * p.N + grow) * 128;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tl + TC_ACC + 64 * h + c0, v);
+        tmem_ld32(acc + c0, v);
         tmem_ld_wait();
         if (grow < p.N) {
 #pragma unroll
@@ -451,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float o0 = __uint_as_float(v[c + 2 * u]) * svh[c0 + c + 2 * u] * inv_l;
-              const float o1 = __uint_as_float(v[c + 2 * u + 1]) * svh[c0 + c + 2 * u + 1] * inv_l;
+              const float o0 = __uint_as_float(v[c + 2 * u]) * s_sv[c0 + c + 2 * u] * inv_l;
+              const float o1 = __uint_as_float(v[c + 2 * u + 1]) * s_sv[c0 + c + 2 * u + 1] * inv_l;
               pk[u] = (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
             }
             *reinterpret_cast<uint4*>(orow + c0 + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -491,11 +519,12 @@ int launch_attention_fp8(uint8_t* S, const vca_state_layout& L, int B, int H, in
   p.B = B; p.H = H; p.N = N; p.nb = nb; p.Npad = Npad;
   p.ngroups = (nb + kGroup - 1) / kGroup;
   p.gpad = p.ngroups * kGroup - nb;
+  p.npairs = (nb + 1) / 2;
   p.qk_scale = (float)(8.0 * 1.4426950408889634 / sqrt(128.0));
   if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return VCA_ERR_CUDA;
-  const long long grid = (long long)BH * nb;
+  const long long grid = (long long)BH * p.npairs;
   if (grid > 0x7FFFFFFF) return VCA_ERR_UNSUPPORTED;
   attn_fp8_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tr, p);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;

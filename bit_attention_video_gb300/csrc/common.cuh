@@ -264,6 +264,38 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_w(uint32_t taddr, uint64_t sd
       "l"(sdesc)
       : "memory");
 }
+// A whole K=128 FP8 product as four K=32 MMAs from one elected lane: the
+// descriptors of steps 1-3 advance the start address by 32 bytes (+2 in the
+// >>4 encoding).  `accum` decides only the first step.
+__device__ __forceinline__ void mma4_f8_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q, t;\n.reg .b64 a1, a2, a3, b1, b2, b3;\n"
+      "elect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\nsetp.eq.u32 t, 0, 0;\n"
+      "add.s64 a1, %1, 2;\nadd.s64 a2, %1, 4;\nadd.s64 a3, %1, 6;\n"
+      "add.s64 b1, %2, 2;\nadd.s64 b2, %2, 4;\nadd.s64 b3, %2, 6;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, q;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, t;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, t;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, t;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// The same with A (four columns of bytes per step: 8 columns) in tensor memory.
+__device__ __forceinline__ void mma4_f8_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p, q, t;\n.reg .b32 a1, a2, a3;\n.reg .b64 b1, b2, b3;\n"
+      "elect.sync _|p, 0xffffffff;\nsetp.ne.u32 q, %4, 0;\nsetp.eq.u32 t, 0, 0;\n"
+      "add.u32 a1, %1, 8;\nadd.u32 a2, %1, 16;\nadd.u32 a3, %1, 24;\n"
+      "add.s64 b1, %2, 2;\nadd.s64 b2, %2, 4;\nadd.s64 b3, %2, 6;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, q;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %3, t;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a2], b2, %3, t;\n"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a3], b3, %3, t;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\n"
