@@ -9,7 +9,8 @@
 //                 and the 16 "slot" rows appended to R^T_j (written by the
 //                 warp's lanes); the mean operand of each group of 8 blocks
 //   warp 1        MMA issuer (warp-uniform loop, one elected lane issues;
-//                 busy-polling) and TMEM owner
+//                 suspending waits, so it takes no issue slots from the
+//                 softmax warps of its SM sub-partition) and TMEM owner
 //   warps 4-7     softmax + correction + epilogue of tile A, warps 8-11 of
 //                 tile B: one thread per query row, which holds the row's 128
 //                 scores in registers (so each SM sub-partition carries one
@@ -248,18 +249,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dstage = kStageBytes >> 4;                          // per-stage step
     const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256);
     const uint64_t dgroup = kGroupBytes >> 4, dhalf = (kGroupBytes / 2) >> 4;
-    bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, p.status);
+    bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
+    // S_X(j); tile B's S(j) reads the stage tile A's S(j) already waited for
     auto issue_s = [&](int X, int j) {
       const int s = j % kStages;
-      ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+      if (X == 0) {
+        ok = mbar_wait(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+      }
       tc_fence_after();
       const uint64_t dk = dk0 + s * dstage, dq = dq0 + X * dqstep;
       mma4_f8_ss_w(tmem + TC_S, dq, dk, i8, 0);
       mma_commit_w(bar(B_SFULL + X));
     };
     auto issue_pv = [&](int X, int j) {
-      ok = mbar_wait_spin(bar(B_PFULL + X), j & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_PFULL + X), j & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
       tc_fence_after();
       const uint64_t dr = dr0 + (j % kStages) * dstage;
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_w(bar(B_PVDONE + X));
     };
     auto wait_sfree = [&](int X, int j) {
-      ok = mbar_wait_spin(bar(B_SFREE + X), j & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_SFREE + X), j & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
     };
     ok = __all_sync(0xffffffffu, ok);
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the last group's mean product, after the softmax read its row sums
     for (int X = 0; ok && X < (has_b ? 2 : 1); ++X) {
-      ok = mbar_wait_spin(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const uint64_t bg = dbg0 + (((nb - 1 + gpad) / kGroup) & 1) * dgroup;
