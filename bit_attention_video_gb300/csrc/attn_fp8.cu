@@ -8,9 +8,12 @@
 //   warp 0        producer: TMA of the two Q tiles once; per stage K'_j, R^T_j
 //                 and the 16 "slot" rows appended to R^T_j (written by the
 //                 warp's lanes); the mean operand of each group of 8 blocks
-//   warp 1        MMA issuer (warp-uniform loop, one elected lane issues;
-//                 suspending waits, so it takes no issue slots from the
-//                 softmax warps of its SM sub-partition) and TMEM owner
+//   warp 1        MMA issuer of the S products (alternating A, B) and TMEM
+//                 owner; warp 2 MMA issuer of the PV products and the stage
+//                 releases.  Warp-uniform loops, one elected lane issues,
+//                 suspending waits.  An mbarrier test costs ~130 cycles even
+//                 on a completed phase, so the two chains of waits run on
+//                 two warps
 //   warps 4-7     softmax + correction + epilogue of tile A, warps 8-11 of
 //                 tile B: one thread per query row, which holds the row's 128
 //                 scores in registers (so each SM sub-partition carries one
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // "S read" and "P written": the 128 softmax threads of a tile; the
     // rest: one arrival or a tcgen05 commit
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 128 : 1);
+      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 128 : (i == B_DRAIN ? 2 : 1));
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmQ);
@@ -235,12 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
     // The whole warp runs this loop (uniform control flow, operands in
     // uniform registers); one elected lane issues each MMA and commit.
-    // Order: S_A(0), S_B(0); per block j: S_A(j+1), PV_A(j), S_B(j+1), PV_B(j)
-    // (each S waits for the other tile to have loaded the shared S buffer).
+    // S issuer: S_A(0), S_B(0), S_A(1), S_B(1), ..., each after the other tile
+    // loaded the shared S buffer.  PV issuer: PV_A(0), PV_B(0), PV_A(1), ...,
+    // each after its tile wrote P; a PV follows its tile's use of the S
+    // product that read the same stage, so its commit releases the stage.
     const uint32_t i8 = idesc_f8(128, 128), i8w = idesc_f8(128, 144), i16 = idesc_bf16(128, 128);
     const uint64_t dq0 = desc_k_sw128(base + OFF_Q);
     const uint64_t dqstep = kTileBytes >> 4;
@@ -282,42 +287,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
     };
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) issue_s(0, 0);
-    if (ok && has_b) {
-      wait_sfree(0, 0);
-      if (ok) issue_s(1, 0);
-    }
-    for (int j = 0; ok && j < nb; ++j) {
-      if (j + 1 < nb) {
-        wait_sfree(has_b ? 1 : 0, j);   // the other tile (or tile A itself) loaded block j
+    if (warp == 1) {
+      // every S product, alternating A, B
+      if (ok) issue_s(0, 0);
+      if (ok && has_b) {
+        wait_sfree(0, 0);
+        if (ok) issue_s(1, 0);
+      }
+      for (int j = 0; ok && j + 1 < nb; ++j) {
+        wait_sfree(has_b ? 1 : 0, j);
         if (!ok) break;
         issue_s(0, j + 1);
         if (!ok) break;
-      }
-      issue_pv(0, j);
-      if (!ok) break;
-      if (has_b) {
-        if (j + 1 < nb) {
+        if (has_b) {
           wait_sfree(0, j + 1);
           if (!ok) break;
           issue_s(1, j + 1);
-          if (!ok) break;
         }
-        issue_pv(1, j);
-        if (!ok) break;
       }
-      mma_commit_w(bar(B_KVEMPTY + j % kStages));
-    }
-    // the last group's mean product, after the softmax read its row sums
-    for (int X = 0; ok && X < (has_b ? 2 : 1); ++X) {
-      ok = mbar_wait(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      const uint64_t bg = dbg0 + (((nb - 1 + gpad) / kGroup) & 1) * dgroup;
-      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg, i16, 1);
-      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_glo(X), bg, i16, 1);
-      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg + dhalf, i16, 1);
-      mma_commit_w(bar(B_PVDONE + X));
+    } else {
+      // every PV product and the stage releases
+      for (int j = 0; ok && j < nb; ++j) {
+        issue_pv(0, j);
+        if (!ok) break;
+        if (has_b) issue_pv(1, j);
+        if (!ok) break;
+        mma_commit_w(bar(B_KVEMPTY + j % kStages));
+      }
+      for (int X = 0; ok && X < (has_b ? 2 : 1); ++X) {
+        ok = mbar_wait(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t bg = dbg0 + (((nb - 1 + gpad) / kGroup) & 1) * dgroup;
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg, i16, 1);
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_glo(X), bg, i16, 1);
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_ghi(X), bg + dhalf, i16, 1);
+        mma_commit_w(bar(B_PVDONE + X));
+      }
     }
     // all issued MMAs complete before the CTA releases its tensor memory
     mma_commit_w(bar(B_DRAIN));
