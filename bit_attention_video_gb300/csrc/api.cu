@@ -65,7 +65,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
                   uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
-                  bool swizzle64) {
+                  int swizzle) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* p = nullptr;
@@ -84,7 +84,9 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t d
       elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            swizzle == 64    ? CU_TENSOR_MAP_SWIZZLE_64B
+            : swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                             : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

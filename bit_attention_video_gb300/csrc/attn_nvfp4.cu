@@ -461,9 +461,9 @@ int launch_attention_nvfp4(uint8_t* S, const vca_state_layout& L, int B, int H, 
                            cudaStream_t st) {
   const int BH = B * H, nb = (N + 127) / 128, Npad = nb * 128;
   CUtensorMap tq, tk, tr;
-  if (!make_tmap_2d(&tq, S + L.q4, 1, 64, (uint64_t)BH * Npad, 64, 64, 128, true) ||
-      !make_tmap_2d(&tk, S + L.k4, 1, 64, (uint64_t)BH * Npad, 64, 64, 128, true) ||
-      !make_tmap_2d(&tr, S + L.r4T, 1, Npad / 2, (uint64_t)BH * 128, Npad / 2, 64, 128, true))
+  if (!make_tmap_2d(&tq, S + L.q4, 1, 64, (uint64_t)BH * Npad, 64, 64, 128, 64) ||
+      !make_tmap_2d(&tk, S + L.k4, 1, 64, (uint64_t)BH * Npad, 64, 64, 128, 64) ||
+      !make_tmap_2d(&tr, S + L.r4T, 1, Npad / 2, (uint64_t)BH * 128, Npad / 2, 64, 128, 64))
     return VCA_ERR_CUDA;
   Nvfp4Params p;
   p.q4s = S + L.q4s;

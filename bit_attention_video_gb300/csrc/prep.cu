@@ -4,6 +4,9 @@
 // single IEEE operation written with an explicit-rounding intrinsic, and every
 // floating-point sum has a fixed order, so codes, scales and means are
 // reproducible bit for bit.
+#include <algorithm>
+#include <cmath>
+
 #include "common.cuh"
 #include "prep.h"
 
@@ -235,47 +238,71 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
   }
 }
 
-// One Lloyd iteration on the tensor cores, for k <= 128.  grid
-// (ceil(N / (128*kTcTiles)), BH), 256 threads.  Per 128-token tile, with the int8 features and centroids
-// held as bf16 (exact for |x| <= 127) and fp32 accumulation (exact: every dot
-// product and every per-CTA sum stays below 2^24):
+// One Lloyd iteration on the tensor cores, for k <= 128.  grid (chunks, BH),
+// 256 threads; a CTA owns a run of 128-token tiles [tile0, tile0 + nt) of one
+// head.  With the int8 features and centroids held as bf16 (exact for
+// |x| <= 127) and fp32 accumulation (exact: every dot product and every
+// per-CTA sum of at most kPipeMaxTiles tiles stays below 2^24), per tile:
 //   D_a = X C^T       (M = 128 tokens, N = kpad centroids, K = 128 channels)
 //   label_t = argmin_m ||c_m||^2 - 2 D_a[t, m]  (lowest index on ties)
 //   D_u += H^T X      (M = 128 cluster rows, N = 128 channels, K = 128 tokens)
 // with H the one-hot label matrix.  The X tile is one shared-memory image:
 // K-major (128-byte swizzle) as the A operand of the first product and
-// MN-major as the B operand of the second.  The CTA's cluster sums D_u and
-// counts are added to the global sums once at the end.
-constexpr int kTcTiles = 8;
-constexpr uint32_t kTcX = 0, kTcH = 32768, kTcC = 65536;  // smem: X, H^T, C (kpad x 256 B)
-inline size_t kmeans_tc_smem_bytes(int kpad) { return kTcC + (size_t)kpad * 256 + 1024 + 2048; }
+// MN-major as the B operand of the second.
+// Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
+// warp 1 MMA issuer and TMEM owner; warps 4-7 workers, one token row per
+// thread, which convert tile t to bf16 while the tensor core works on tile
+// t-1 and then take tile t-1's argmin and write its one-hot columns.  X, H^T
+// and D_a are double-buffered.  The CTA's cluster sums D_u and counts are
+// added to the global sums once at the end.
+constexpr int kPipeStages = 3;
+constexpr int kPipeMaxTiles = 1024;                   // 1024 * 128 * 127 < 2^24
+constexpr uint32_t kPX = 0;                           // X bf16: 2 x 32 KB
+constexpr uint32_t kPH = 65536;                       // H^T bf16: 2 x 32 KB
+constexpr uint32_t kPS = 131072;                      // int8 tiles: kPipeStages x 16 KB
+constexpr uint32_t kPC = kPS + kPipeStages * 16384;   // centroids bf16: kpad x 256 B
+inline size_t kmeans_pipe_smem_bytes(int kpad) { return kPC + (size_t)kpad * 256 + 1024; }
 
-__global__ void __launch_bounds__(256) kmeans_assign_tc_kernel(const int8_t* x, const int8_t* cent,
-                                                               int32_t* labels, int32_t* sums,
-                                                               int32_t* counts, int N, int k,
-                                                               int kpad, const int* status) {
+// barrier indices
+enum { KB_XFULL = 0, KB_XEMPTY = KB_XFULL + kPipeStages, KB_XREADY = KB_XEMPTY + kPipeStages,
+       KB_DA = KB_XREADY + 2, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
+       KB_CNT = KB_UDONE + 2, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
+
+__global__ void __launch_bounds__(256, 1)
+    kmeans_assign_pipe_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t* cent,
+                              int32_t* labels, int32_t* sums, int32_t* counts, int N, int k,
+                              int kpad, int tiles_per_cta, int* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bars[KB_COUNT];
   __shared__ int abort_flag;
-  __shared__ int32_t cnt[256];
-  __shared__ int32_t cnorm[256];
+  __shared__ int32_t cnt[128];
+  __shared__ int32_t cnorm[128];
   if (prep_skip(status)) return;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base - raw);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int bh = blockIdx.y, tile0 = blockIdx.x * kTcTiles;
-  const int ntile_head = (N + 127) / 128;
-  const int ntiles = min(kTcTiles, ntile_head - tile0);
-  const uint32_t ncols = kpad <= 128 ? 256 : 512, col_u = kpad <= 128 ? 128 : 256;
-  if (warp == 0) {
+  const int bh = blockIdx.y;
+  const int tile0 = blockIdx.x * tiles_per_cta;
+  const int nt = min(tiles_per_cta, (N + 127) / 128 - tile0);
+  if (nt <= 0) return;  // uniform over the CTA
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t ncols = kpad <= 64 ? 256 : 512;
+  const uint32_t col_u = kpad <= 64 ? 128 : 256;  // D_u; D_a[b] at b * kpad
+  if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_slot), ncols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(smem_u32(&bar), 1);
+    for (int i = 0; i < KB_COUNT; ++i) {
+      const bool workers = (i >= KB_XEMPTY && i < KB_XREADY + 2) ||
+                           (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
+      mbar_init(bar(i), workers ? 128 : 1);
+    }
     abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tensormap(&tmX);
   }
   // centroids -> bf16, K-major 128-byte swizzle: two atoms of kpad rows x 64
   // channels; rows k..kpad-1 are zero
@@ -289,14 +316,13 @@ __global__ void __launch_bounds__(256) kmeans_assign_tc_kernel(const int8_t* x, 
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float f = (float)(int8_t)((sv[e / 4] >> (8 * (e % 4))) & 0xFF);
-        const uint32_t bits = f32_to_bf16_bits(f);
-        w[e / 2] |= bits << (16 * (e % 2));
+        w[e / 2] |= (__float_as_uint(f) >> 16) << (16 * (e % 2));
       }
     }
-    *reinterpret_cast<uint4*>(sm + kTcC + atom * kpad * 128 + m * 128 + ((ch ^ (m & 7)) << 4)) =
+    *reinterpret_cast<uint4*>(sm + kPC + atom * kpad * 128 + m * 128 + ((ch ^ (m & 7)) << 4)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
-  for (int m = tid; m < 256; m += 256) {
+  for (int m = tid; m < 128; m += 256) {
     cnt[m] = 0;
     int32_t n2 = 0;
     if (m < k)
@@ -306,112 +332,185 @@ __global__ void __launch_bounds__(256) kmeans_assign_tc_kernel(const int8_t* x, 
       }
     cnorm[m] = n2;
   }
+  // both one-hot buffers start at zero; a worker later clears only the entry
+  // it set two tiles before
+  for (int i = tid; i < 2 * 32768 / 16; i += 256)
+    reinterpret_cast<uint4*>(sm + kPH)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t ia = idesc_bf16(128, kpad), iu = idesc_bf16(128, 128, true);
-  uint32_t phase = 0;
-  bool ok = true;
-  for (int tt = 0; tt < ntiles && ok; ++tt) {
-    const int t0 = (tile0 + tt) * 128;
-    // X tile: token rows, bf16, K-major swizzled; H^T tile cleared
-    const int8_t* xg = x + ((size_t)bh * N + t0) * 128;
-    for (int i = tid; i < 128 * 16; i += 256) {
-      const int t = i / 16, c8 = i % 16, atom = c8 / 8, ch = c8 % 8;
-      uint32_t w[4] = {0, 0, 0, 0};
-      if (t0 + t < N) {
-        const uint2 src = *reinterpret_cast<const uint2*>(xg + (size_t)t * 128 + c8 * 8);
-        const uint32_t sv[2] = {src.x, src.y};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float f = (float)(int8_t)((sv[e / 4] >> (8 * (e % 4))) & 0xFF);
-          w[e / 2] |= (uint32_t)f32_to_bf16_bits(f) << (16 * (e % 2));
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    int issued = 0;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % kPipeStages;
+      if (t >= kPipeStages)
+        ok = mbar_wait(bar(KB_XEMPTY + s), ((t / kPipeStages) - 1) & 1, &abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane == 0) {
+        mbar_expect_tx(bar(KB_XFULL + s), 16384);
+        tma_load_2d(base + kPS + s * 16384, &tmX, bar(KB_XFULL + s), 0,
+                    bh * N + (tile0 + t) * 128);
+      }
+      ++issued;
+    }
+    if (lane == 0 && abort_flag) {
+      // let the copies in flight land before the CTA exits
+      const uint64_t t0 = globaltimer();
+      for (int t = max(0, issued - kPipeStages); t < issued; ++t) {
+        const int s = t % kPipeStages;
+        while (!mbar_try_wait(bar(KB_XFULL + s), (t / kPipeStages) & 1) &&
+               globaltimer() - t0 < kWaitLimitNs) {
         }
       }
-      *reinterpret_cast<uint4*>(sm + kTcX + atom * 16384 + t * 128 + ((ch ^ (t & 7)) << 4)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(sm + kTcH)[i] = make_uint4(0, 0, 0, 0);
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) {
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // per step t: assign(t) once tile t is converted, update(t-1) once its
+    // one-hot columns are written
+    const uint32_t ia = idesc_bf16(128, kpad), iu = idesc_bf16(128, 128, true);
+    bool ok = true;
+    for (int t = 0; t <= nt && ok; ++t) {
+      if (t < nt) {
+        const int b = t & 1;
+        ok = mbar_wait(bar(KB_XREADY + b), (t >> 1) & 1, &abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t xb = base + kPX + b * 32768;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
-        const uint32_t oc = (s / 4) * kpad * 128 + (s % 4) * 32;
-        mma_f16_ss_w(tmem, desc_k_sw128(base + kTcX + o), desc_k_sw128(base + kTcC + oc), ia, s > 0);
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
+          const uint32_t oc = (s / 4) * kpad * 128 + (s % 4) * 32;
+          mma_f16_ss_w(tmem + b * kpad, desc_k_sw128(xb + o), desc_k_sw128(base + kPC + oc), ia,
+                       s > 0);
+        }
+        mma_commit_w(bar(KB_DA + b));
       }
-      mma_commit_w(smem_u32(&bar));
+      if (t >= 1) {
+        const int u = t - 1, b = u & 1;
+        ok = mbar_wait(bar(KB_HREADY + b), (u >> 1) & 1, &abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t xb = base + kPX + b * 32768, hb = base + kPH + b * 32768;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_f16_ss_w(tmem + col_u, desc_k_sw128(hb + (s / 4) * 16384 + (s % 4) * 32),
+                       make_desc(xb + s * 2048, 16384, 1024, 2), iu, (u > 0 || s > 0));
+        mma_commit_w(bar(KB_UDONE + b));
+      }
     }
-    ok = mbar_wait(smem_u32(&bar), phase, &abort_flag, const_cast<int*>(status));
-    phase ^= 1;
-    tc_fence_after();
-    if (warp < 4 && __all_sync(0xffffffffu, ok)) {
-      // one token per thread: its row of D_a
-      const int t = warp * 32 + lane;
-      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-      int best = 0x7FFFFFFF, bestm = 0;
-      for (int c0 = 0; c0 < kpad; c0 += 32) {
+    // every issued product completes before the CTA releases its tensor memory
+    mma_commit_w(bar(KB_DRAIN));
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar(KB_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ workers
+    const int wt = tid - 128, quarter = warp - 4;  // token row / cluster row = TMEM lane
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
+    bool ok = true;
+    for (int t = 0; t <= nt && ok; ++t) {
+      if (t < nt) {
+        // convert tile t: int8 rows (no swizzle) -> bf16 K-major 128-byte
+        // swizzle (channels 0-63 and 64-127 in two 16 KB atoms)
+        const int s = t % kPipeStages, b = t & 1;
+        ok = mbar_wait(bar(KB_XFULL + s), (t / kPipeStages) & 1, &abort_flag, status);
+        if (ok && t >= 2) ok = mbar_wait(bar(KB_UDONE + b), ((t - 2) >> 1) & 1, &abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t* src = sm + kPS + s * 16384;
+        uint8_t* xb = sm + kPX + b * 32768;
+#pragma unroll 2
+        for (int u = 0; u < 8; ++u) {
+          const int i = wt + 128 * u, r = i >> 3, c = i & 7;  // row r, 16 channels from 16 c
+          const uint4 in = *reinterpret_cast<const uint4*>(src + r * 128 + c * 16);
+          const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float f0 = (float)(int8_t)((iw[e / 4] >> (8 * (e % 4))) & 0xFF);
+            const float f1 = (float)(int8_t)((iw[e / 4] >> (8 * (e % 4 + 1))) & 0xFF);
+            w[e / 2] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xFFFF0000u);
+          }
+          uint8_t* dst = xb + (c >> 2) * 16384 + r * 128;
+          const int ch = (c & 3) * 2;
+          *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (r & 7)) << 4)) =
+              make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(KB_XEMPTY + s));
+        mbar_arrive(bar(KB_XREADY + b));
+      }
+      if (t >= 1) {
+        // tile t-1: argmin of this token's row of D_a, then its one-hot column
+        const int u = t - 1, b = u & 1;
+        ok = mbar_wait(bar(KB_DA + b), (u >> 1) & 1, &abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t trow = tmem + lanes + b * kpad;
+        int best = 0x7FFFFFFF, bestm = 0;
+        for (int c0 = 0; c0 < kpad; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(trow + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int m = c0 + c;
+            if (m < k) {
+              const int dist = cnorm[m] - 2 * (int)__uint_as_float(v[c]);
+              if (dist < best) { best = dist; bestm = m; }
+            }
+          }
+        }
+        const int token = (tile0 + u) * 128 + wt;
+        uint8_t* hb = sm + kPH + b * 32768;
+        // H^T[m][token] at (token / 64) * 16 KB + m * 128 B, 16-byte chunk
+        // (token % 64) / 8 swizzled with m % 8, element token % 8
+        auto hoff = [&](int m) {
+          return (wt / 64) * 16384 + m * 128 + ((((wt % 64) / 8) ^ (m & 7)) << 4) + (wt % 8) * 2;
+        };
+        if (old_lab[b] >= 0) *reinterpret_cast<uint16_t*>(hb + hoff(old_lab[b])) = 0;
+        old_lab[b] = -1;
+        if (token < N) {
+          labels[(size_t)bh * N + token] = bestm;
+          atomicAdd(&cnt[bestm], 1);
+          *reinterpret_cast<uint16_t*>(hb + hoff(bestm)) = 0x3F80;  // 1.0
+          old_lab[b] = bestm;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(KB_HREADY + b));
+      }
+    }
+    // the CTA's cluster sums (TMEM lane m = cluster m) and counts
+    mbar_arrive(bar(KB_CNT));
+    if (ok) ok = mbar_wait(bar(KB_UDONE + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, &abort_flag, status);
+    if (ok) ok = mbar_wait(bar(KB_CNT), 0, &abort_flag, status);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int m = wt;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(trow + c0, v);
+        tmem_ld32(tmem + lanes + col_u + c0, v);
         tmem_ld_wait();
+        if (m < k && cnt[m] > 0)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int m = c0 + c;
-          const int dist = cnorm[min(m, 255)] - 2 * (int)__uint_as_float(v[c]);
-          if (m < k && dist < best) { best = dist; bestm = m; }
-        }
+          for (int c = 0; c < 32; ++c) {
+            const int sv = (int)__uint_as_float(v[c]);
+            if (sv) atomicAdd(&sums[((size_t)bh * k + m) * 128 + c0 + c], sv);
+          }
       }
-      if (t0 + t < N) {
-        labels[(size_t)bh * N + t0 + t] = bestm;
-        atomicAdd(&cnt[bestm], 1);
-        // H^T[bestm][t] = 1.0 (bf16), K-major swizzled over the token axis
-        const int atom = t / 64, c8 = (t % 64) / 8, e = t % 8;
-        *reinterpret_cast<uint16_t*>(sm + kTcH + atom * 16384 + bestm * 128 +
-                                     ((c8 ^ (bestm & 7)) << 4) + e * 2) = 0x3F80;
-      }
-    }
-    if (!__syncthreads_and(ok)) break;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) {
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        mma_f16_ss_w(tmem + col_u, desc_k_sw128(base + kTcH + (s / 4) * 16384 + (s % 4) * 32),
-                     make_desc(base + kTcX + s * 2048, 16384, 1024, 2), iu, (tt > 0 || s > 0));
-      mma_commit_w(smem_u32(&bar));
-    }
-    ok = mbar_wait(smem_u32(&bar), phase, &abort_flag, const_cast<int*>(status));
-    phase ^= 1;
-    tc_fence_after();
-    ok = __syncthreads_and(ok);
-  }
-  if (ok && ntiles > 0 && warp < 4) {
-    // cluster row m = TMEM lane m of D_u
-    const int m = warp * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + col_u;
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(trow + c0, v);
-      tmem_ld_wait();
-      if (m < k && cnt[m] > 0)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int sv = (int)__uint_as_float(v[c]);
-          if (sv) atomicAdd(&sums[((size_t)bh * k + m) * 128 + c0 + c], sv);
-        }
+      if (m < k && cnt[m]) atomicAdd(&counts[(size_t)bh * k + m], cnt[m]);
     }
   }
-  __syncthreads();
-  for (int m = tid; m < k; m += 256)
-    if (cnt[m]) atomicAdd(&counts[(size_t)bh * k + m], cnt[m]);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
@@ -931,7 +1030,7 @@ inline int grid_chunks(size_t work, int per_block, int cap) {
 // ---------------------------------------------------------------------------
 // Header, grouping (skipped when the cached permutation is reused) and the
 // key channel mean: the part of the chain both bit widths share.
-static void launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
+static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   const int BH = a.B * a.H, N = a.N, nb = a.nb, k = a.k;
   const size_t per_head = (size_t)N * 128;
   uint8_t* S = a.state;
@@ -957,15 +1056,34 @@ static void launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
     features_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
     kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
     if (k <= 128) {
-      // tensor-core Lloyd iteration (the cluster-sum product has M = 128 rows)
+      // tensor-core Lloyd iteration (the cluster-sum product has M = 128 rows):
+      // each CTA takes a run of tiles of one head, runs sized to fill whole
+      // waves of the SMs (and short enough for exact fp32 sums)
       const int kpad = (k + 15) / 16 * 16;
-      const size_t tsmem = kmeans_tc_smem_bytes(kpad);
-      cudaFuncSetAttribute(kmeans_assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tsmem);
-      const int tiles = ((N + 127) / 128 + kTcTiles - 1) / kTcTiles;
+      const size_t psmem = kmeans_pipe_smem_bytes(kpad);
+      cudaFuncSetAttribute(kmeans_assign_pipe_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+      CUtensorMap tmx;
+      if (!make_tmap_2d(&tmx, x, 1, 128, (uint64_t)BH * N, 128, 128, 128, 0)) return VCA_ERR_CUDA;
+      int dev = 0, nsm = 152;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+      const int T = (N + 127) / 128;
+      int tpc = std::min(T, kPipeMaxTiles);
+      double best = 1e300;
+      for (int c = 1; c <= 4 * nsm; ++c) {
+        const int run = (T + c - 1) / c;
+        if (run <= kPipeMaxTiles) {
+          const double waves = std::ceil((double)((T + run - 1) / run) * BH / nsm);
+          const double cost = waves * (run + 4);  // + the per-CTA set-up, in tiles
+          if (cost < best) { best = cost; tpc = run; }
+        }
+        if (run == 1) break;
+      }
+      const dim3 grid((T + tpc - 1) / tpc, BH);
       for (int it = 0; it < a.iters; ++it) {
-        kmeans_assign_tc_kernel<<<dim3(tiles, BH), 256, tsmem, st>>>(x, cent, labels, sums,
-                                                                     counts, N, k, kpad, status);
+        kmeans_assign_pipe_kernel<<<grid, 256, psmem, st>>>(tmx, cent, labels, sums, counts, N,
+                                                             k, kpad, tpc, status);
         kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
       }
     } else {
@@ -992,6 +1110,7 @@ static void launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   float* ksum = reinterpret_cast<float*>(S + L.ksum);
   key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
   key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
+  return VCA_OK;
 }
 
 int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
@@ -1004,7 +1123,7 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   const uint16_t* kk = a.k_in;
   const uint16_t* v = a.v;
   const int32_t* perm = reinterpret_cast<const int32_t*>(S + L.perm);
-  launch_front(a, 8, st);
+  if (const int rc = launch_front(a, 8, st); rc != VCA_OK) return rc;
   uint8_t* qhat = S + L.qhat;
   float* sq = reinterpret_cast<float*>(S + L.sq);
   uint8_t* khat = S + L.khat;
@@ -1040,7 +1159,7 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   const uint16_t* kk = a.k_in;
   const uint16_t* v = a.v;
   const int32_t* perm = reinterpret_cast<const int32_t*>(S + L.perm);
-  launch_front(a, 4, st);
+  if (const int rc = launch_front(a, 4, st); rc != VCA_OK) return rc;
   const uint16_t* kbar = reinterpret_cast<const uint16_t*>(S + L.kbar);
   uint16_t* mu = reinterpret_cast<uint16_t*>(S + L.mu);
   float* vamax = reinterpret_cast<float*>(S + L.vamax);

@@ -50,10 +50,9 @@ int launch_attention_bf16(const void* q, const void* k, const void* v, int B, in
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 // 2-D tensor of `elem_bytes`-byte elements: inner extent `dim0`, `dim1` rows of
-// `row_bytes` bytes, box (box0, box1), 128-byte swizzle (64-byte when
-// `swizzle64`).
+// `row_bytes` bytes, box (box0, box1); `swizzle` = 128, 64 (bytes) or 0 (none).
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
                   uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
-                  bool swizzle64 = false);
+                  int swizzle = 128);
 
 }  // namespace vca
