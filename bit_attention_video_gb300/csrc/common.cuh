@@ -318,6 +318,10 @@ __host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major = false) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -439,6 +443,15 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
   return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFF)));
 }
 
+// Four int8 (one word, byte i = element i) -> two f16x2 words, exactly:
+// byte b is placed as the half 1024 + (b ^ 0x80) (exponent 10, so the low
+// mantissa bits are the byte) and 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x5342);
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float((uint32_t)b << 16);
 }

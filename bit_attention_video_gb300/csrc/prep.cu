@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 
 // One Lloyd iteration on the tensor cores, for k <= 128.  grid (chunks, BH),
 // 256 threads; a CTA owns a run of 128-token tiles [tile0, tile0 + nt) of one
-// head.  With the int8 features and centroids held as bf16 (exact for
+// head.  With the int8 features and centroids held as fp16 (exact for
 // |x| <= 127) and fp32 accumulation (exact: every dot product and every
 // per-CTA sum of at most kPipeMaxTiles tiles stays below 2^24), per tile:
 //   D_a = X C^T       (M = 128 tokens, N = kpad centroids, K = 128 channels)
@@ -251,33 +251,37 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 // MN-major as the B operand of the second.
 // Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
 // warp 1 MMA issuer and TMEM owner; warps 4-7 workers, one token row per
-// thread, which convert tile t to bf16 while the tensor core works on tile
-// t-1 and then take tile t-1's argmin and write its one-hot columns.  X, H^T
-// and D_a are double-buffered.  The CTA's cluster sums D_u and counts are
-// added to the global sums once at the end.
+// thread, which convert tile t to fp16 while the tensor core works on tile
+// t-1 and then take tile t-1's argmin and write its one-hot columns.  H^T and
+// D_a are double-buffered and X has nx = 3 buffers when shared memory allows
+// (2 otherwise), so converting a tile waits for the cluster-sum product of
+// the tile nx before it, issued an iteration earlier.  The CTA's cluster sums
+// D_u and counts are added to the global sums once at the end.
 constexpr int kPipeStages = 3;
 constexpr int kPipeMaxTiles = 1024;                   // 1024 * 128 * 127 < 2^24
-constexpr uint32_t kPX = 0;                           // X bf16: 2 x 32 KB
-constexpr uint32_t kPH = 65536;                       // H^T bf16: 2 x 32 KB
-constexpr uint32_t kPS = 131072;                      // int8 tiles: kPipeStages x 16 KB
-constexpr uint32_t kPC = kPS + kPipeStages * 16384;   // centroids bf16: kpad x 256 B
-inline size_t kmeans_pipe_smem_bytes(int kpad) { return kPC + (size_t)kpad * 256 + 1024; }
+// shared memory: X bf16 nx x 32 KB | H^T bf16 2 x 32 KB | int8 tiles
+// kPipeStages x 16 KB | centroids bf16 kpad x 256 B
+constexpr uint32_t kPipeStaticSmem = 2048;            // the kernel's static shared memory, rounded up
+__host__ __device__ inline uint32_t kpipe_h(int nx) { return nx * 32768u; }
+__host__ __device__ inline uint32_t kpipe_s(int nx) { return kpipe_h(nx) + 65536u; }
+__host__ __device__ inline uint32_t kpipe_c(int nx) { return kpipe_s(nx) + kPipeStages * 16384u; }
+inline size_t kmeans_pipe_smem_bytes(int kpad, int nx) { return kpipe_c(nx) + (size_t)kpad * 256 + 1024; }
 
 // barrier indices
 enum { KB_XFULL = 0, KB_XEMPTY = KB_XFULL + kPipeStages, KB_XREADY = KB_XEMPTY + kPipeStages,
-       KB_DA = KB_XREADY + 2, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
-       KB_CNT = KB_UDONE + 2, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
+       KB_DA = KB_XREADY + 3, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
+       KB_CNT = KB_UDONE + 3, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
 
 __global__ void __launch_bounds__(256, 1)
     kmeans_assign_pipe_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t* cent,
                               int32_t* labels, int32_t* sums, int32_t* counts, int N, int k,
-                              int kpad, int tiles_per_cta, int* status) {
+                              int kpad, int tiles_per_cta, int nx, int* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t bars[KB_COUNT];
   __shared__ int abort_flag;
   __shared__ int32_t cnt[128];
-  __shared__ int32_t cnorm[128];
+  __shared__ float cnorm[128];  // ||c_m||^2, an integer below 2^24
   if (prep_skip(status)) return;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -288,6 +292,7 @@ __global__ void __launch_bounds__(256, 1)
   const int nt = min(tiles_per_cta, (N + 127) / 128 - tile0);
   if (nt <= 0) return;  // uniform over the CTA
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t kPX = 0, kPH = kpipe_h(nx), kPS = kpipe_s(nx), kPC = kpipe_c(nx);
   const uint32_t ncols = kpad <= 64 ? 256 : 512;
   const uint32_t col_u = kpad <= 64 ? 128 : 256;  // D_u; D_a[b] at b * kpad
   if (warp == 1) {
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(256, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < KB_COUNT; ++i) {
-      const bool workers = (i >= KB_XEMPTY && i < KB_XREADY + 2) ||
+      const bool workers = (i >= KB_XEMPTY && i < KB_XREADY + 3) ||
                            (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
       mbar_init(bar(i), workers ? 128 : 1);
     }
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(256, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmX);
   }
-  // centroids -> bf16, K-major 128-byte swizzle: two atoms of kpad rows x 64
+  // centroids -> fp16, K-major 128-byte swizzle: two atoms of kpad rows x 64
   // channels; rows k..kpad-1 are zero
   const int8_t* cg = cent + (size_t)bh * k * 128;
   for (int i = tid; i < kpad * 16; i += 256) {  // one 16-byte chunk (8 channels) per step
@@ -312,12 +317,8 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t w[4] = {0, 0, 0, 0};
     if (m < k) {
       const uint2 src = *reinterpret_cast<const uint2*>(cg + (size_t)m * 128 + c8 * 8);
-      const uint32_t sv[2] = {src.x, src.y};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float f = (float)(int8_t)((sv[e / 4] >> (8 * (e % 4))) & 0xFF);
-        w[e / 2] |= (__float_as_uint(f) >> 16) << (16 * (e % 2));
-      }
+      i8x4_to_f16x4(src.x, w[0], w[1]);
+      i8x4_to_f16x4(src.y, w[2], w[3]);
     }
     *reinterpret_cast<uint4*>(sm + kPC + atom * kpad * 128 + m * 128 + ((ch ^ (m & 7)) << 4)) =
         make_uint4(w[0], w[1], w[2], w[3]);
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(256, 1)
         const int v = cg[(size_t)m * 128 + c];
         n2 += v * v;
       }
-    cnorm[m] = n2;
+    cnorm[m] = (float)n2;
   }
   // both one-hot buffers start at zero; a worker later clears only the entry
   // it set two tiles before
@@ -372,15 +373,15 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ MMA issuer
     // per step t: assign(t) once tile t is converted, update(t-1) once its
     // one-hot columns are written
-    const uint32_t ia = idesc_bf16(128, kpad), iu = idesc_bf16(128, 128, true);
+    const uint32_t ia = idesc_f16(128, kpad), iu = idesc_f16(128, 128, true);
     bool ok = true;
     for (int t = 0; t <= nt && ok; ++t) {
       if (t < nt) {
-        const int b = t & 1;
-        ok = mbar_wait(bar(KB_XREADY + b), (t >> 1) & 1, &abort_flag, status);
+        const int b = t & 1, xi = t % nx;
+        ok = mbar_wait(bar(KB_XREADY + xi), (t / nx) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t xb = base + kPX + b * 32768;
+        const uint32_t xb = base + kPX + xi * 32768;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t o = (s / 4) * 16384 + (s % 4) * 32;
@@ -395,12 +396,12 @@ __global__ void __launch_bounds__(256, 1)
         ok = mbar_wait(bar(KB_HREADY + b), (u >> 1) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t xb = base + kPX + b * 32768, hb = base + kPH + b * 32768;
+        const uint32_t xb = base + kPX + (u % nx) * 32768, hb = base + kPH + b * 32768;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_f16_ss_w(tmem + col_u, desc_k_sw128(hb + (s / 4) * 16384 + (s % 4) * 32),
                        make_desc(xb + s * 2048, 16384, 1024, 2), iu, (u > 0 || s > 0));
-        mma_commit_w(bar(KB_UDONE + b));
+        mma_commit_w(bar(KB_UDONE + u % nx));
       }
     }
     // every issued product completes before the CTA releases its tensor memory
@@ -416,14 +417,15 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (int t = 0; t <= nt && ok; ++t) {
       if (t < nt) {
-        // convert tile t: int8 rows (no swizzle) -> bf16 K-major 128-byte
+        // convert tile t: int8 rows (no swizzle) -> fp16 K-major 128-byte
         // swizzle (channels 0-63 and 64-127 in two 16 KB atoms)
-        const int s = t % kPipeStages, b = t & 1;
+        const int s = t % kPipeStages, xi = t % nx;
         ok = mbar_wait(bar(KB_XFULL + s), (t / kPipeStages) & 1, &abort_flag, status);
-        if (ok && t >= 2) ok = mbar_wait(bar(KB_UDONE + b), ((t - 2) >> 1) & 1, &abort_flag, status);
+        // X[xi] was last read by the cluster-sum product of tile t - nx
+        if (ok && t >= nx) ok = mbar_wait(bar(KB_UDONE + xi), ((t / nx) - 1) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t* src = sm + kPS + s * 16384;
-        uint8_t* xb = sm + kPX + b * 32768;
+        uint8_t* xb = sm + kPX + xi * 32768;
 #pragma unroll 2
         for (int u = 0; u < 8; ++u) {
           const int i = wt + 128 * u, r = i >> 3, c = i & 7;  // row r, 16 channels from 16 c
@@ -431,11 +433,7 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
           uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float f0 = (float)(int8_t)((iw[e / 4] >> (8 * (e % 4))) & 0xFF);
-            const float f1 = (float)(int8_t)((iw[e / 4] >> (8 * (e % 4 + 1))) & 0xFF);
-            w[e / 2] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xFFFF0000u);
-          }
+          for (int q = 0; q < 4; ++q) i8x4_to_f16x4(iw[q], w[2 * q], w[2 * q + 1]);
           uint8_t* dst = xb + (c >> 2) * 16384 + r * 128;
           const int ch = (c & 3) * 2;
           *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -444,16 +442,21 @@ __global__ void __launch_bounds__(256, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(KB_XEMPTY + s));
-        mbar_arrive(bar(KB_XREADY + b));
+        mbar_arrive(bar(KB_XREADY + xi));
       }
       if (t >= 1) {
         // tile t-1: argmin of this token's row of D_a, then its one-hot column
         const int u = t - 1, b = u & 1;
         ok = mbar_wait(bar(KB_DA + b), (u >> 1) & 1, &abort_flag, status);
+        // H^T[b] was last read by the cluster-sum product of tile u - 2
+        if (ok && u >= 2) ok = mbar_wait(bar(KB_UDONE + (u - 2) % nx), ((u - 2) / nx) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint32_t trow = tmem + lanes + b * kpad;
-        int best = 0x7FFFFFFF, bestm = 0;
+        // distances ||c||^2 - 2 x.c are integers below 2^24: exact in fp32;
+        // the strict comparison keeps the lowest index on ties
+        float best = INFINITY;
+        int bestm = 0;
         for (int c0 = 0; c0 < kpad; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(trow + c0, v);
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(256, 1)
           for (int c = 0; c < 32; ++c) {
             const int m = c0 + c;
             if (m < k) {
-              const int dist = cnorm[m] - 2 * (int)__uint_as_float(v[c]);
+              const float dist = fmaf(-2.0f, __uint_as_float(v[c]), cnorm[m]);
               if (dist < best) { best = dist; bestm = m; }
             }
           }
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(256, 1)
         if (token < N) {
           labels[(size_t)bh * N + token] = bestm;
           atomicAdd(&cnt[bestm], 1);
-          *reinterpret_cast<uint16_t*>(hb + hoff(bestm)) = 0x3F80;  // 1.0
+          *reinterpret_cast<uint16_t*>(hb + hoff(bestm)) = 0x3C00;  // 1.0 (fp16)
           old_lab[b] = bestm;
         }
         fence_proxy_async_smem();
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     // the CTA's cluster sums (TMEM lane m = cluster m) and counts
     mbar_arrive(bar(KB_CNT));
-    if (ok) ok = mbar_wait(bar(KB_UDONE + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, &abort_flag, status);
+    if (ok) ok = mbar_wait(bar(KB_UDONE + (nt - 1) % nx), ((nt - 1) / nx) & 1, &abort_flag, status);
     if (ok) ok = mbar_wait(bar(KB_CNT), 0, &abort_flag, status);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
@@ -1060,7 +1063,8 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
       // each CTA takes a run of tiles of one head, runs sized to fill whole
       // waves of the SMs (and short enough for exact fp32 sums)
       const int kpad = (k + 15) / 16 * 16;
-      const size_t psmem = kmeans_pipe_smem_bytes(kpad);
+      const int nx = kmeans_pipe_smem_bytes(kpad, 3) + kPipeStaticSmem <= 232448 ? 3 : 2;
+      const size_t psmem = kmeans_pipe_smem_bytes(kpad, nx);
       cudaFuncSetAttribute(kmeans_assign_pipe_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
       CUtensorMap tmx;
@@ -1083,7 +1087,7 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
       const dim3 grid((T + tpc - 1) / tpc, BH);
       for (int it = 0; it < a.iters; ++it) {
         kmeans_assign_pipe_kernel<<<grid, 256, psmem, st>>>(tmx, cent, labels, sums, counts, N,
-                                                             k, kpad, tpc, status);
+                                                             k, kpad, tpc, nx, status);
         kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
       }
     } else {
