@@ -256,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dgroup = kGroupBytes >> 4, dhalf = (kGroupBytes / 2) >> 4;
     bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
     // S_X(j); tile B's S(j) reads the stage tile A's S(j) already waited for
-    auto issue_s = [&](int X, int j) {
+    auto issue_s = [&](int X, int j, bool kv_ready = false) {
       const int s = j % kStages;
-      if (X == 0) {
+      if (X == 0 && !kv_ready) {
         ok = mbar_wait(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
       }
@@ -295,9 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) issue_s(1, 0);
       }
       for (int j = 0; ok && j + 1 < nb; ++j) {
+        // the stage of block j+1 first (usually landed long before), so the
+        // wait for the other tile is the last step before the product
+        ok = mbar_wait(bar(B_KVFULL + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag,
+                       p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         wait_sfree(has_b ? 1 : 0, j);
         if (!ok) break;
-        issue_s(0, j + 1);
+        issue_s(0, j + 1, true);
         if (!ok) break;
         if (has_b) {
           wait_sfree(0, j + 1);
