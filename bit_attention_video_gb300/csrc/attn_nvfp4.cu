@@ -8,35 +8,43 @@
 // microscale), so the softmax evaluates the exponential, and P is quantised to
 // NVFP4 after scaling the row so that its maximum is 448 * 6 = 2688.
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams the key
-// blocks through a TMA ring.  Warp roles as in the 8-bit kernel:
-//   warp 0        producer: Q tile and its scales once; per stage K'_j, R^T_j
-//                 and their two scale tiles; the mean operand of each group
-//                 of 4 blocks (ring of 4)
-//   warp 1        MMA issuer (warp-uniform, elected lane) and TMEM owner; it
-//                 also copies every scale tile into tensor memory
-//                 (tcgen05.cp), in order with the products that read it
-//   warps 4-11    softmax + correction + epilogue: two threads per query row
-//                 (keys / output channels 0-63 and 64-127)
+// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and
+// streams the key blocks through a TMA ring; both tiles consume each stage.
+// Warp roles (12 warps):
+//   warp 0      producer: the two Q tiles and their scales once; per stage K'_j,
+//               R^T_j and their two scale tiles; the mean operand of each
+//               group of 4 blocks (ring of 4)
+//   warp 1      S issuer and TMEM owner: copies the Q scales once and the K'
+//               scales of each block into tensor memory (tcgen05.cp), then
+//               issues S_A(j), S_B(j), S_A(j+1), ... each after the other tile
+//               loaded the shared S buffer
+//   warp 2      PV issuer: copies the R and P scales, issues PV_A(j), PV_B(j)
+//               and the mean products, and releases the stages
+//   warps 4-7   softmax + correction + epilogue of tile A, warps 8-11 of tile
+//               B, one thread per query row (the row's 128 scores in registers)
+// Every scale copy is issued by the warp whose products read it, so the copy
+// and the products execute in issue order.
 //
 // Tensor memory (480 of 512 columns):
-//   [0,128), [128,256)  S_j = Q K'_j^T (raw, without gq gk) in buffer j % 2
-//   [256,384)  the output accumulator A
-//   [384,392)  Q scale factors (two K steps x 4 columns)
-//   [392,400)  P scale factors
-//   [400,408)  a group's row-sum operand (bf16 hi, lo) of the mean product
-//   [416,480)  K' and R scale factors of block j in slot j % 4 (16 columns)
+//   [0,128)     S = Q K'^T (raw, without gq gk), shared by the two tiles
+//   [128,384)   the output accumulators A_A, A_B
+//   [384,400)   Q scale factors of A, B (two K steps x 4 columns each)
+//   [400,416)   P scale factors of A, B
+//   [416,432)   a group's row-sum operand (bf16 hi, lo) of A, B
+//   [432,448)   K' scale factors, two slots (blocks j % 2)
+//   [448,464)   R scale factors, two slots
 //
-// Per key block j (log2 domain, a = gq gk log2(e) / sqrt(d)):
+// Per key block j and tile (log2 domain, a = gq gk log2(e) / sqrt(d)):
 //   M'  = max(M, a rowmax(S))
 //   p'  = 2^(a S - M' + log2 2688)          so that p' <= 2688
 //   r   = sum p'   (fp32, from the unquantised probabilities: Eq 6's r)
-//   P   = NVFP4(p'): scale UE4M3(max16 / 6), elements E2M1(p' / scale)
+//   P   = NVFP4(p'): scale UE4M3(max16 / 6), elements E2M1(p' / scale), each
+//         element evaluated directly as 2^(a S - M' + log2 2688 - log2 scale)
 //   A  *= alpha = 2^(M - M'), l = alpha l + r
 //   A  += P R_j          (block-scaled FP4 MMA; R = R-codes x scales, no gr)
-//   A  += (r / gr) mu_j  (one BF16 K=16 MMA per group of 4 blocks; each of
-//                         the two threads of a row contributes its own partial
-//                         sums as separate K entries, hi/lo split)
+//   A  += (r / gr) mu_j  (one BF16 K=16 MMA per group of 4 blocks; the bf16 hi
+//                         and lo of each block's rescaled row sum meet the
+//                         block's mean in K rows 2u, 2u+1)
 // Epilogue: O = gr A / l (l in the same 2688-scaled units), bf16.
 #include "common.cuh"
 #include "prep.h"
@@ -47,23 +55,25 @@ namespace {
 constexpr int kStages = 8;
 constexpr int kMeanBufs = 4;
 constexpr uint32_t kStageBytes = 2 * kTile4Bytes + 2 * kScaleTileBytes;  // K', R^T, scales
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_QS = OFF_Q + kTile4Bytes;
-constexpr uint32_t OFF_KV = OFF_QS + kScaleTileBytes;
-constexpr uint32_t OFF_P = OFF_KV + kStages * kStageBytes;
-constexpr uint32_t OFF_PS = OFF_P + kTile4Bytes;
-constexpr uint32_t OFF_BG = OFF_PS + kScaleTileBytes;
-constexpr uint32_t OFF_XCH = OFF_BG + kMeanBufs * kGroup4Bytes;  // partial row max, 2 x 2 x 128
-constexpr uint32_t OFF_L = OFF_XCH + 2048;                       // partial row sums, 2 x 128
-constexpr uint32_t OFF_BAR = OFF_L + 1024;
+constexpr uint32_t OFF_Q = 0;                                 // Q_A, Q_B
+constexpr uint32_t OFF_QS = OFF_Q + 2 * kTile4Bytes;          // their scale tiles
+constexpr uint32_t OFF_KV = OFF_QS + 2 * kScaleTileBytes;
+constexpr uint32_t OFF_P = OFF_KV + kStages * kStageBytes;    // P_A, P_B
+constexpr uint32_t OFF_PS = OFF_P + 2 * kTile4Bytes;          // their scale tiles
+constexpr uint32_t OFF_BG = OFF_PS + 2 * kScaleTileBytes;
+constexpr uint32_t OFF_BAR = OFF_BG + kMeanBufs * kGroup4Bytes;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
 constexpr int kThreads = 384;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0,
               "swizzled tiles stay 1024-byte aligned");
-static_assert(kGroup4 == 4, "four row-sum slots per thread");
+static_assert(kGroup4 == 4, "four row-sum slots per group");
 
-constexpr uint32_t TC_S = 0, TC_ACC = 256, TC_QS = 384, TC_PS = 392, TC_G = 400, TC_KRS = 416;
+constexpr uint32_t TC_S = 0, TC_KS = 432, TC_RS = 448;
+__device__ __forceinline__ uint32_t tc_acc(int X) { return 128u + 128u * X; }
+__device__ __forceinline__ uint32_t tc_qs(int X) { return 384u + 8u * X; }
+__device__ __forceinline__ uint32_t tc_ps(int X) { return 400u + 8u * X; }
+__device__ __forceinline__ uint32_t tc_g(int X) { return 416u + 8u * X; }
 
 struct Nvfp4Params {
   const uint8_t* q4s;     // [BH][nb][1024]
@@ -73,24 +83,23 @@ struct Nvfp4Params {
   const uint32_t* hdr;
   uint16_t* out;          // [BH][N][128]
   int* status;
-  int B, H, N, nb, Npad, ngroups, gpad;
+  int B, H, N, nb, Npad, ngroups, gpad, npairs;
   float log2e_rsqrt_d;    // log2(e) / sqrt(128)
 };
 
 enum { B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = B_KVFULL + kStages, B_SFULL = B_KVEMPTY + kStages,
-       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 1,
-       B_DRAIN = B_PVDONE + 1, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4 };
+       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2,
+       B_DRAIN = B_PVDONE + 2, B_COUNT = B_DRAIN + 1 };
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ bool group_ends(int j, int nb, int gpad) {
@@ -111,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nb = p.nb, gpad = p.gpad;
-  const int bh = blockIdx.x / nb, qt = blockIdx.x % nb;
+  const int bh = blockIdx.x / p.npairs, qp = blockIdx.x % p.npairs;
+  const bool has_b = 2 * qp + 1 < nb;   // the last pair of an odd nb has tile A only
 
   {
     const volatile uint32_t* h = p.hdr;
@@ -125,11 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (threadIdx.x == 0) {
-    // "S read" and "P written": all 256 softmax threads; the row-pair
-    // exchange of each lane quarter: its two warps; the rest: one arrival
-    // or a tcgen05 commit
+    // "S read" and "P written": the 128 softmax threads of a tile; the drain:
+    // both issuers; the rest: one arrival or a tcgen05 commit
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 256 : (i >= B_XCH ? 64 : 1));
+      mbar_init(bar(i), (i >= B_SFREE && i < B_PVDONE) ? 128 : (i == B_DRAIN ? 2 : 1));
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmQ);
@@ -144,15 +153,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t i4 = idesc_nvf4(128, 128);
+  const uint64_t dstage = kStageBytes >> 4, dhalf = 512 >> 4;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     bool ok = true;
     if (lane == 0) {
-      mbar_expect_tx(bar(B_QFULL), kTile4Bytes + kScaleTileBytes);
-      tma_load_2d(base + OFF_Q, &tmQ, bar(B_QFULL), 0, bh * p.Npad + qt * 128);
-      bulk_load(base + OFF_QS, p.q4s + ((size_t)bh * nb + qt) * kScaleTileBytes, kScaleTileBytes,
-                bar(B_QFULL));
+      mbar_expect_tx(bar(B_QFULL), (has_b ? 2 : 1) * (kTile4Bytes + kScaleTileBytes));
+      for (int X = 0; X < (has_b ? 2 : 1); ++X) {
+        tma_load_2d(base + OFF_Q + X * kTile4Bytes, &tmQ, bar(B_QFULL), 0,
+                    bh * p.Npad + (2 * qp + X) * 128);
+        bulk_load(base + OFF_QS + X * kScaleTileBytes,
+                  p.q4s + ((size_t)bh * nb + 2 * qp + X) * kScaleTileBytes, kScaleTileBytes,
+                  bar(B_QFULL));
+      }
     }
     int issued = 0;
     for (int j = 0; j < nb; ++j) {
@@ -191,198 +206,243 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t i4 = idesc_nvf4(128, 128), i16 = idesc_bf16(128, 128);
-    const uint64_t dq = desc_k_sw64(base + OFF_Q);
-    const uint64_t dp = desc_k_sw64(base + OFF_P);
+    // ------------------------------------------------------------ S issuer
+    const uint64_t dq0 = desc_k_sw64(base + OFF_Q), dqstep = kTile4Bytes >> 4;
     const uint64_t dk0 = desc_k_sw64(base + OFF_KV);
-    const uint64_t dr0 = desc_k_sw64(base + OFF_KV + kTile4Bytes);
-    const uint64_t dstage = kStageBytes >> 4;
-    // scale tiles: 32 rows x 16 bytes per K step, no swizzle
-    const uint64_t dqs = desc_k_plain(base + OFF_QS, 512, 128);
-    const uint64_t dps = desc_k_plain(base + OFF_PS, 512, 128);
+    const uint64_t dqs0 = desc_k_plain(base + OFF_QS, 512, 128);
     const uint64_t dks0 = desc_k_plain(base + OFF_KV + 2 * kTile4Bytes, 512, 128);
-    const uint64_t dhalf = 512 >> 4, dtile = kScaleTileBytes >> 4;
-    const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256);
-    const uint64_t dgroup = kGroup4Bytes >> 4;
-    bool ok = mbar_wait_spin(bar(B_QFULL), 0, abort_flag, p.status);
+    const uint64_t dtile = kScaleTileBytes >> 4;
+    bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      tmem_cp_32x128b_x4_w(tmem + TC_QS, dqs);
-      tmem_cp_32x128b_x4_w(tmem + TC_QS + 4, dqs + dhalf);
+      for (int X = 0; X < (has_b ? 2 : 1); ++X) {
+        tmem_cp_32x128b_x4_w(tmem + tc_qs(X), dqs0 + X * dtile);
+        tmem_cp_32x128b_x4_w(tmem + tc_qs(X) + 4, dqs0 + X * dtile + dhalf);
+      }
     } else {
       ok = false;
     }
-    auto issue_s = [&](int j) {
+    // S_X(j); tile A's product also copies the block's K' scales (slot j % 2)
+    auto issue_s = [&](int X, int j, bool kv_ready) {
       const int s = j % kStages;
-      ok = mbar_wait_spin(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
-      tc_fence_after();
-      const uint32_t krs = tmem + TC_KRS + 16 * (j % 4);
-      const uint64_t ds = dks0 + s * dstage;
-      tmem_cp_32x128b_x4_w(krs, ds);                       // K' scales, K step 0
-      tmem_cp_32x128b_x4_w(krs + 4, ds + dhalf);           // K' scales, K step 1
-      tmem_cp_32x128b_x4_w(krs + 8, ds + dtile);           // R scales, K step 0
-      tmem_cp_32x128b_x4_w(krs + 12, ds + dtile + dhalf);  // R scales, K step 1
-      const uint64_t dk = dk0 + s * dstage;
-      const uint32_t d = tmem + TC_S + 128 * (j & 1);
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        mma_nvf4_ss_w(d, dq + 2 * kk, dk + 2 * kk, i4, tmem + TC_QS + 4 * kk, krs + 4 * kk, kk > 0);
-      mma_commit_w(bar(B_SFULL + (j & 1)));
-    };
-    auto issue_flush = [&](int g) {
-      mma_f16_ts_w(tmem + TC_ACC, tmem + TC_G, dbg0 + (g % kMeanBufs) * dgroup, i16, 1);
-    };
-    for (int j = 0; ok && j < min(2, nb); ++j) issue_s(j);
-    for (int j = 0; ok && j < nb; ++j) {
-      ok = mbar_wait_spin(bar(B_PFULL), j & 1, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      tmem_cp_32x128b_x4_w(tmem + TC_PS, dps);
-      tmem_cp_32x128b_x4_w(tmem + TC_PS + 4, dps + dhalf);
-      const uint64_t dr = dr0 + (j % kStages) * dstage;
-      const uint32_t krs = tmem + TC_KRS + 16 * (j % 4);
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        mma_nvf4_ss_w(tmem + TC_ACC, dp + 2 * kk, dr + 2 * kk, i4, tmem + TC_PS + 4 * kk,
-                      krs + 8 + 4 * kk, (j > 0 || kk > 0));
-      if (j > 0 && group_ends(j - 1, nb, gpad)) issue_flush((j - 1 + gpad) / kGroup4);
-      mma_commit_w(bar(B_PVDONE));
-      mma_commit_w(bar(B_KVEMPTY + j % kStages));
-      if (j + 2 < nb) {
-        ok = mbar_wait_spin(bar(B_SFREE + (j & 1)), (j >> 1) & 1, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        issue_s(j + 2);
-      }
-    }
-    if (ok) {
-      ok = mbar_wait_spin(bar(B_PFULL), nb & 1, abort_flag, p.status);
-      if (__all_sync(0xffffffffu, ok)) {
+      if (X == 0) {
+        if (!kv_ready) {
+          ok = mbar_wait(bar(B_KVFULL + s), (j / kStages) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+        }
         tc_fence_after();
-        issue_flush((nb - 1 + gpad) / kGroup4);
-        mma_commit_w(bar(B_PVDONE));
+        tmem_cp_32x128b_x4_w(tmem + TC_KS + 8 * (j & 1), dks0 + s * dstage);
+        tmem_cp_32x128b_x4_w(tmem + TC_KS + 8 * (j & 1) + 4, dks0 + s * dstage + dhalf);
+      } else {
+        tc_fence_after();
+      }
+      const uint64_t dk = dk0 + s * dstage, dq = dq0 + X * dqstep;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        mma_nvf4_ss_w(tmem + TC_S, dq + 2 * kk, dk + 2 * kk, i4, tmem + tc_qs(X) + 4 * kk,
+                      tmem + TC_KS + 8 * (j & 1) + 4 * kk, kk > 0);
+      mma_commit_w(bar(B_SFULL + X));
+    };
+    auto wait_sfree = [&](int X, int j) {
+      ok = mbar_wait(bar(B_SFREE + X), j & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+    };
+    if (ok) issue_s(0, 0, false);
+    if (ok && has_b) {
+      wait_sfree(0, 0);
+      if (ok) issue_s(1, 0, true);
+    }
+    for (int j = 0; ok && j + 1 < nb; ++j) {
+      // the stage of block j+1 first (usually landed long before), so the wait
+      // for the other tile is the last step before the product
+      ok = mbar_wait(bar(B_KVFULL + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag,
+                     p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      wait_sfree(has_b ? 1 : 0, j);
+      if (!ok) break;
+      issue_s(0, j + 1, true);
+      if (!ok) break;
+      if (has_b) {
+        wait_sfree(0, j + 1);
+        if (!ok) break;
+        issue_s(1, j + 1, true);
       }
     }
     mma_commit_w(bar(B_DRAIN));
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
     }
-  } else if (warp >= 4) {
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    const uint64_t dp0 = desc_k_sw64(base + OFF_P), dpstep = kTile4Bytes >> 4;
+    const uint64_t dr0 = desc_k_sw64(base + OFF_KV + kTile4Bytes);
+    const uint64_t dps0 = desc_k_plain(base + OFF_PS, 512, 128), dtile = kScaleTileBytes >> 4;
+    const uint64_t drs0 = desc_k_plain(base + OFF_KV + 2 * kTile4Bytes + kScaleTileBytes, 512, 128);
+    const uint64_t dbg0 = desc_k_plain(base + OFF_BG, 128, 256), dgroup = kGroup4Bytes >> 4;
+    const uint32_t i16 = idesc_bf16(128, 128);
+    bool ok = true;
+    auto issue_pv = [&](int X, int j) {
+      ok = mbar_wait(bar(B_PFULL + X), j & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; return; }
+      tc_fence_after();
+      const int s = j % kStages;
+      if (X == 0) {  // the block's R scales (slot j % 2), used by both tiles
+        tmem_cp_32x128b_x4_w(tmem + TC_RS + 8 * (j & 1), drs0 + s * dstage);
+        tmem_cp_32x128b_x4_w(tmem + TC_RS + 8 * (j & 1) + 4, drs0 + s * dstage + dhalf);
+      }
+      tmem_cp_32x128b_x4_w(tmem + tc_ps(X), dps0 + X * dtile);
+      tmem_cp_32x128b_x4_w(tmem + tc_ps(X) + 4, dps0 + X * dtile + dhalf);
+      const uint64_t dr = dr0 + s * dstage, dp = dp0 + X * dpstep;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        mma_nvf4_ss_w(tmem + tc_acc(X), dp + 2 * kk, dr + 2 * kk, i4, tmem + tc_ps(X) + 4 * kk,
+                      tmem + TC_RS + 8 * (j & 1) + 4 * kk, (j > 0 || kk > 0));
+      if (j > 0 && group_ends(j - 1, nb, gpad))
+        mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_g(X),
+                     dbg0 + (((j - 1 + gpad) / kGroup4) % kMeanBufs) * dgroup, i16, 1);
+      mma_commit_w(bar(B_PVDONE + X));
+    };
+    for (int j = 0; ok && j < nb; ++j) {
+      issue_pv(0, j);
+      if (!ok) break;
+      if (has_b) issue_pv(1, j);
+      if (!ok) break;
+      mma_commit_w(bar(B_KVEMPTY + j % kStages));
+    }
+    // the last group's mean product, after the softmax wrote its row sums
+    for (int X = 0; ok && X < (has_b ? 2 : 1); ++X) {
+      ok = mbar_wait(bar(B_PFULL + X), nb & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      mma_f16_ts_w(tmem + tc_acc(X), tmem + tc_g(X),
+                   dbg0 + (((nb - 1 + gpad) / kGroup4) % kMeanBufs) * dgroup, i16, 1);
+      mma_commit_w(bar(B_PVDONE + X));
+    }
+    mma_commit_w(bar(B_DRAIN));
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+    }
+  } else if (warp >= 4 && (warp < 8 || has_b)) {
     // ------------------------------------------------------------ softmax
-    const int h = (warp - 4) / 4, quarter = warp % 4;
-    const int row = quarter * 32 + lane;
+    const int X = (warp - 4) / 4, quarter = warp % 4;
+    const int qt = 2 * qp + X;
+    const int row = quarter * 32 + lane;  // row within the query tile = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    // The two threads of a row exchange partial results through shared memory
-    // and the quarter's mbarrier (bounded waits, so a stalled partner cannot
-    // hang the CTA); phase j is block j, phase nb the final normaliser.
-    const uint32_t xbar = bar(B_XCH + quarter);
+    const uint32_t acc = tl + tc_acc(X);
     const float gq = p.g4[(size_t)bh * 4], gk = p.g4[(size_t)bh * 4 + 1];
     const float gr = p.g4[(size_t)bh * 4 + 2];
     const float a = gq * gk * p.log2e_rsqrt_d;
     const float inv_gr = 1.0f / gr;
     const float kLog2P = 11.392317f;          // log2(2688)
-    const int valid_last = p.N - (nb - 1) * 128 - 64 * h;
-    float* xch_base = reinterpret_cast<float*>(sm + OFF_XCH);
-    uint8_t* ptile = sm + OFF_P;
-    uint32_t* pscale = reinterpret_cast<uint32_t*>(sm + OFF_PS + h * 512 + (row % 32) * 16 +
-                                                   (row / 32) * 4);
+    const int valid_last = p.N - (nb - 1) * 128;
+    uint8_t* ptile = sm + OFF_P + X * kTile4Bytes;
+    // this row's scale words: K step 0 (keys 0-63) and, 512 bytes on, step 1
+    uint32_t* ps = reinterpret_cast<uint32_t*>(sm + OFF_PS + X * kScaleTileBytes +
+                                               (row % 32) * 16 + (row / 32) * 4);
     float M = -INFINITY, l = 0.0f;
     float pend[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = true;
-    // the row-sum operand of a group: column 4h + u = bf16 (hi, lo) of this
-    // thread's rescaled partial sum of slot u, divided by gr
+    // the row-sum operand of a group: column u = bf16 (hi, lo) of the
+    // rescaled row sum of slot u divided by gr; columns 4-7 (K 8..15) zero
     auto write_group = [&]() {
-      uint32_t w[4];
+      uint32_t w[8];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float x = pend[u] * inv_gr;
         const uint16_t hi = f32_to_bf16_bits(x);
         const uint16_t lo = f32_to_bf16_bits(x - bf16_bits_to_f32(hi));
         w[u] = (uint32_t)hi | ((uint32_t)lo << 16);
+        w[4 + u] = 0u;
         pend[u] = 0.0f;
       }
-      tmem_st4(tl + TC_G + 4 * h, w);
+      tmem_st8(tl + tc_g(X), w);
     };
     for (int j = 0; j < nb; ++j) {
-      const uint32_t sbuf = tl + TC_S + 128 * (j & 1);
-      ok = mbar_wait(bar(B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_SFULL + X), j & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t s[64];
-      tmem_ld32(sbuf + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(sbuf + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      // all 128 scores of the row into registers, then release the S buffer
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tl + TC_S + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_SFREE + (j & 1)));
-      if (j == nb - 1 && valid_last < 64) {
+      mbar_arrive(bar(B_SFREE + X));
+      if (j == nb - 1 && valid_last < 128) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 128; ++c)
           if (c >= valid_last) s[c] = 0xFF800000u;  // -inf: masked key -> probability 0
       }
-      float mx16[4];
+      float mx16[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float m = __uint_as_float(s[16 * i]);
+      for (int i = 0; i < 8; ++i) {
+        float m = fmaxf(__uint_as_float(s[16 * i]), __uint_as_float(s[16 * i + 15]));
 #pragma unroll
-        for (int c = 1; c < 16; ++c) m = fmaxf(m, __uint_as_float(s[16 * i + c]));
+        for (int c = 1; c < 15; c += 2)
+          m = max3(m, __uint_as_float(s[16 * i + c]), __uint_as_float(s[16 * i + c + 1]));
         mx16[i] = m;
       }
-      float* xch = xch_base + (j & 1) * 256;
-      xch[h * 128 + row] = fmaxf(fmaxf(mx16[0], mx16[1]), fmaxf(mx16[2], mx16[3]));
-      mbar_arrive(xbar);
-      ok = mbar_wait_spin(xbar, j & 1, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const float mx = fmaxf(xch[row], xch[128 + row]);
+      const float mx = fmaxf(fmaxf(max3(mx16[0], mx16[1], mx16[2]), max3(mx16[3], mx16[4], mx16[5])),
+                             fmaxf(mx16[6], mx16[7]));
       const float Mn = fmaxf(M, a * mx);
       const float alpha = ex2(M - Mn);   // 0 on the first block
       const float nbias = kLog2P - Mn;
-      // p' = 2688 * 2^(a s - M'), its sum, and the NVFP4 codes of each 16
+      // Per 16 keys: the block scale from the block maximum, then each code
+      // straight from q = p' / scale = 2^(a s - M' + log2 2688 - log2 scale)
+      // (one FMA and one ex2 per score); the row sum r = sum p' is rebuilt as
+      // scale * sum q per block of 16.  A block whose scale rounds to zero
+      // holds probabilities below 2688 * 2^-10 / 6 of the maximum: codes 0,
+      // and their negligible share of r is dropped.
       float rs = 0.0f;
-      uint32_t pw[8];
-      uint32_t sc4 = 0;
+      uint32_t pw[16];
+      uint32_t sc4[2] = {0u, 0u};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const float amax = ex2(fmaf(mx16[i], a, nbias));
         const uint32_t sc = f32_to_e4m3(amax * (1.0f / 6.0f));
         const float scv = e4m3_to_f32((uint8_t)sc);
-        const float inv = scv > 0.0f ? 1.0f / scv : 0.0f;
-        sc4 |= sc << (8 * i);
-        uint32_t w0 = 0, w1 = 0;
+        float l2s;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2s) : "f"(scv));
+        const float nbi = scv > 0.0f ? nbias - l2s : -INFINITY;
+        sc4[i / 4] |= sc << (8 * (i % 4));
+        float rsi = 0.0f;
+        uint32_t by[8];
 #pragma unroll
         for (int c = 0; c < 16; c += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[16 * i + c]), a, nbias));
-          const float p1 = ex2(fmaf(__uint_as_float(s[16 * i + c + 1]), a, nbias));
-          rs += p0 + p1;
-          const uint32_t byte = f32x2_to_e2m1x2(p0 * inv, p1 * inv);
-          if (c < 8) w0 |= byte << (4 * c);
-          else w1 |= byte << (4 * (c - 8));
+          const float q0 = ex2(fmaf(__uint_as_float(s[16 * i + c]), a, nbi));
+          const float q1 = ex2(fmaf(__uint_as_float(s[16 * i + c + 1]), a, nbi));
+          rsi += q0 + q1;
+          by[c / 2] = f32x2_to_e2m1x2(q0, q1);
         }
-        pw[2 * i] = w0;
-        pw[2 * i + 1] = w1;
+        rs = fmaf(rsi, scv, rs);
+        pw[2 * i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+        pw[2 * i + 1] = __byte_perm(__byte_perm(by[4], by[5], 0x0040), __byte_perm(by[6], by[7], 0x0040), 0x5410);
       }
       if (j > 0) {
-        ok = mbar_wait(bar(B_PVDONE), (j - 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(bar(B_PVDONE + X), (j - 1) & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
-      // P codes (64-byte swizzled K-major, this half = 16-byte chunks 2h, 2h+1)
-      // and the four P scales of this half
-      *reinterpret_cast<uint4*>(ptile + off_sw64(row, 2 * h)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      *reinterpret_cast<uint4*>(ptile + off_sw64(row, 2 * h + 1)) =
-          make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      *pscale = sc4;
+      // P codes (64-byte swizzled K-major: 16-byte chunk c = keys 32c..32c+31)
+      // and the row's eight P scales
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(ptile + off_sw64(row, c)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      ps[0] = sc4[0];
+      ps[128] = sc4[1];
       fence_proxy_async_smem();
       if (j > 0) {
         if (__any_sync(0xffffffffu, alpha < 1.0f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
+          for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tl + TC_ACC + 64 * h + c0, v);
+            tmem_ld32(acc + c0, v);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-            tmem_st32(tl + TC_ACC + 64 * h + c0, v);
+            tmem_st32(acc + c0, v);
           }
         }
 #pragma unroll
@@ -396,39 +456,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       M = Mn;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + X));
     }
     if (ok) {
-      ok = mbar_wait(bar(B_PVDONE), (nb - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(bar(B_PVDONE + X), (nb - 1) & 1, abort_flag, p.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         write_group();
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
-        ok = mbar_wait(bar(B_PVDONE), nb & 1, abort_flag, p.status);
+        mbar_arrive(bar(B_PFULL + X));
+        ok = mbar_wait(bar(B_PVDONE + X), nb & 1, abort_flag, p.status);
       } else {
         ok = false;
       }
     }
-    // the row's normaliser: this half's sum plus the partner's
-    float* lx = reinterpret_cast<float*>(sm + OFF_L);
-    float ltot = 0.0f;
-    if (__all_sync(0xffffffffu, ok)) {
-      lx[h * 128 + row] = l;
-      mbar_arrive(xbar);
-      ok = mbar_wait_spin(xbar, nb & 1, abort_flag, p.status);
-      ltot = lx[row] + lx[128 + row];
-    }
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int grow = qt * 128 + row;
-      const float f = gr / ltot;
-      uint16_t* orow = p.out + ((size_t)bh * p.N + grow) * 128 + 64 * h;
+      const float f = gr / l;
+      uint16_t* orow = p.out + ((size_t)bh * p.N + grow) * 128;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tl + TC_ACC + 64 * h + c0, v);
+        tmem_ld32(acc + c0, v);
         tmem_ld_wait();
         if (grow < p.N) {
 #pragma unroll
@@ -476,11 +527,12 @@ int launch_attention_nvfp4(uint8_t* S, const vca_state_layout& L, int B, int H, 
   p.B = B; p.H = H; p.N = N; p.nb = nb; p.Npad = Npad;
   p.ngroups = (nb + kGroup4 - 1) / kGroup4;
   p.gpad = p.ngroups * kGroup4 - nb;
+  p.npairs = (nb + 1) / 2;
   p.log2e_rsqrt_d = (float)(1.4426950408889634 / sqrt(128.0));
   if (cudaFuncSetAttribute(attn_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return VCA_ERR_CUDA;
-  const long long grid = (long long)BH * nb;
+  const long long grid = (long long)BH * p.npairs;
   if (grid > 0x7FFFFFFF) return VCA_ERR_UNSUPPORTED;
   attn_nvfp4_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tr, p);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
