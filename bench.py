@@ -38,13 +38,17 @@ NOMINAL_TFLOPS = {8: 4500.0, 4: 13500.0}
 PER_BF16 = {8: 2.0, 4: 6.0}
 PEAK_NAME = {8: "fp8", 4: "fp4"}
 
-# DRAM bytes (read + write) of one FP8 attention launch, from one ncu capture
-# of the sweep16k workload (B1 H24 N16384): 154.6 MB read + 70.0 MB written.
-# Every row of Q, K, R and O crosses DRAM once, so the figure scales with the
-# token count.  It holds only for the kernel source it was captured on.
-ATTN_TRAFFIC = dict(bytes=154.639104e6 + 69.965568e6, tokens=24 * 16384,
-                    sources={"attn_fp8.cu": "d7f0ef868e92f6c2375a39a9a5ddb5ed2204053767769bd774274cda81f2a72e",
-                             "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"})
+# DRAM bytes (read + write) of one attention launch, from one ncu capture of
+# the 16384-token, 24-head workload per bit width.  Every row of Q, K, R and
+# O crosses DRAM once, so the figure scales with the token count.  It holds
+# only for the kernel source it was captured on.
+ATTN_TRAFFIC = {
+    8: dict(bytes=154.310144e6 + 67.740928e6, tokens=24 * 16384,
+            sources={"attn_fp8.cu": "fb292866b4acb3e45af602ba3c6b4bc0bab4bbae0fd6fde654eb34c66c5b23a3",
+                     "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"}),
+    4: dict(bytes=88.280320e6 + 52.350976e6, tokens=24 * 16384,
+            sources={"attn_nvfp4.cu": "d6a319a3ebc46b74895063894dba3d4f453e5cbd32d3ceeea567c3fc340ac539"}),
+}
 
 
 def peaks():
@@ -61,14 +65,13 @@ def attn_traffic(w):
     """Scaled DRAM traffic of one attention launch, or None if the kernel
     source differs from the one the counters were taken on."""
     import hashlib
+    ref = ATTN_TRAFFIC[w.bits]
     csrc = os.path.join(ROOT, "bit_attention_video_gb300", "csrc")
-    for name, digest in ATTN_TRAFFIC["sources"].items():
+    for name, digest in ref["sources"].items():
         with open(os.path.join(csrc, name), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != digest:
                 return None
-    if w.bits != 8:
-        return None     # the 4-bit kernel has no capture yet
-    return ATTN_TRAFFIC["bytes"] * (w.B * w.H * w.N) / ATTN_TRAFFIC["tokens"]
+    return ref["bytes"] * (w.B * w.H * w.N) / ref["tokens"]
 
 
 def vsmooth_bytes(w, iters: int, reuse: bool) -> float:

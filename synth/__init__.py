@@ -73,6 +73,8 @@ CONFIGS = {
     "sweep128k": Workload("sweep_B1_H24_N131072", 1, 24, 131072, 128, 64, 64, 8, 0xC0FFEE + 4),
     "wan720p_fp4": Workload("wan720p_nvfp4_B1_H40_N75600", 1, 40, 75600, 128, 64, 64, 4,
                             0xC0FFEE + 5),
+    "sweep16k_fp4": Workload("sweep_nvfp4_B1_H24_N16384", 1, 24, 16384, 128, 64, 64, 4,
+                             0xC0FFEE + 5),
 }
 
 
