@@ -107,7 +107,9 @@ def launches_per_step(iters: int, reuse: bool, bits: int = 8) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (100 ms) during the timed region.  Entering waits
+    (at most 5 s) for the first sample, so that the sampler is running before
+    the region starts, and drops it: every kept sample falls inside."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -120,10 +122,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t_end = time.monotonic() + 5.0
+            while not self.rows and time.monotonic() < t_end and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.rows.clear()
         except OSError:
             self.proc = None
         return self
@@ -417,7 +423,7 @@ def run_gpu(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="wan720p", choices=sorted(synth.CONFIGS))
