@@ -96,6 +96,8 @@ def _declare(L):
                                           C.c_int, _P]
     L.orc_kmeans.restype = None
     L.orc_kmeans.argtypes = [_P, C.POINTER(HeadCfg), _P, _P, _P, _P]
+    L.orc_kmeans_warm.restype = None
+    L.orc_kmeans_warm.argtypes = [_P, C.POINTER(HeadCfg), _P, C.c_float, _P, _P, _P, _P]
     L.orc_stable_argsort.restype = None
     L.orc_stable_argsort.argtypes = [_P, C.c_int, C.c_int, _P]
     L.orc_block_demean.restype = None
@@ -212,6 +214,26 @@ def kmeans(v_head: np.ndarray, k: int, iters: int, seed: int, b=0, h=0, H=1):
     labels = np.zeros(N, np.int32)
     cent = np.zeros((k, d), np.int8)
     lib().orc_kmeans(_ptr(v), C.byref(cfg), _ptr(x), _ptr(gs), _ptr(labels), _ptr(cent))
+    return x, float(gs[0]), labels, cent
+
+
+def kmeans_warm(v_head: np.ndarray, prev_centroids: np.ndarray, prev_grid_scale: float,
+                iters: int):
+    """Warm-started k-means of one head from the previous step's centroids and
+    grid scale.  Returns (x int8 [N,d], grid_scale, labels, centroids); with
+    iters = 0 the centroids are the previous ones moved to the new grid and
+    the labels are -1."""
+    v = _c(v_head, np.uint16)
+    N, d = v.shape
+    prev = _c(prev_centroids, np.int8)
+    k = prev.shape[0]
+    cfg = _cfg(N, d, k, iters, 8, 0, 0, 0, 1)
+    x = np.zeros((N, d), np.int8)
+    gs = np.zeros(1, np.float32)
+    labels = np.full(N, -1, np.int32)
+    cent = np.zeros((k, d), np.int8)
+    lib().orc_kmeans_warm(_ptr(v), C.byref(cfg), _ptr(prev), float(prev_grid_scale), _ptr(x),
+                          _ptr(gs), _ptr(labels), _ptr(cent))
     return x, float(gs[0]), labels, cent
 
 

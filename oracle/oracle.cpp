@@ -213,34 +213,27 @@ void orc_kmeans_init_indices(uint64_t seed, int b, int h, int H, int N, int k, i
   }
 }
 
-void orc_kmeans(const uint16_t* v, const orc_head_cfg* cfg, int8_t* x_out, float* grid_scale_out,
-                int32_t* labels, int8_t* centroids) {
-  const int N = cfg->N, d = cfg->d, k = cfg->k;
-  // Features: the value tokens on a symmetric int8 grid with one scale per head.
+// Features: the value tokens on a symmetric int8 grid with one scale per head,
+// s = amax / 127 (1 for an all-zero head), x = clamp(RNE(v / s), -127, 127).
+static float kmeans_features(const uint16_t* v, int N, int d, std::vector<int>& x) {
   float amax = 0.0f;
   for (size_t i = 0; i < (size_t)N * d; ++i) amax = std::max(amax, std::fabs(bf(v[i])));
-  float s = amax > 0.0f ? amax / 127.0f : 1.0f;
-  std::vector<int> x((size_t)N * d);
+  const float s = amax > 0.0f ? amax / 127.0f : 1.0f;
+  x.assign((size_t)N * d, 0);
   for (size_t i = 0; i < (size_t)N * d; ++i) {
     float q = std::nearbyintf(bf(v[i]) / s);
     x[i] = (int)std::min(127.0f, std::max(-127.0f, q));
   }
-  if (x_out)
-    for (size_t i = 0; i < x.size(); ++i) x_out[i] = (int8_t)x[i];
-  *grid_scale_out = s;
+  return s;
+}
 
-  // Initial centroids: k distinct tokens chosen by SplitMix64.
-  std::vector<int32_t> idx(k);
-  orc_kmeans_init_indices(cfg->seed, cfg->b, cfg->h, cfg->H, N, k, idx.data());
-  std::vector<int> c((size_t)k * d);
-  for (int m = 0; m < k; ++m)
-    for (int j = 0; j < d; ++j) c[(size_t)m * d + j] = x[(size_t)idx[m] * d + j];
-
-  // Lloyd iterations: assign to the nearest centroid (squared Euclidean
-  // distance, lowest index on ties), then move each centroid to the
-  // round-half-even integer mean of its members; an empty cluster keeps its
-  // centroid.  The labels are those of the last assignment.
-  for (int it = 0; it < cfg->iters; ++it) {
+// Lloyd iterations: assign to the nearest centroid (squared Euclidean
+// distance, lowest index on ties), then move each centroid to the
+// round-half-even integer mean of its members; an empty cluster keeps its
+// centroid.  The labels are those of the last assignment.
+static void kmeans_lloyd(const std::vector<int>& x, int N, int d, int k, int iters,
+                         std::vector<int>& c, int32_t* labels) {
+  for (int it = 0; it < iters; ++it) {
     for (int t = 0; t < N; ++t) {
       int64_t best = 0;
       int bestm = -1;
@@ -264,6 +257,47 @@ void orc_kmeans(const uint16_t* v, const orc_head_cfg* cfg, int8_t* x_out, float
         for (int j = 0; j < d; ++j)
           c[(size_t)m * d + j] = (int)div_round_half_even(sum[(size_t)m * d + j], cnt[m]);
   }
+}
+
+void orc_kmeans(const uint16_t* v, const orc_head_cfg* cfg, int8_t* x_out, float* grid_scale_out,
+                int32_t* labels, int8_t* centroids) {
+  const int N = cfg->N, d = cfg->d, k = cfg->k;
+  std::vector<int> x;
+  const float s = kmeans_features(v, N, d, x);
+  if (x_out)
+    for (size_t i = 0; i < x.size(); ++i) x_out[i] = (int8_t)x[i];
+  *grid_scale_out = s;
+
+  // Initial centroids: k distinct tokens chosen by SplitMix64.
+  std::vector<int32_t> idx(k);
+  orc_kmeans_init_indices(cfg->seed, cfg->b, cfg->h, cfg->H, N, k, idx.data());
+  std::vector<int> c((size_t)k * d);
+  for (int m = 0; m < k; ++m)
+    for (int j = 0; j < d; ++j) c[(size_t)m * d + j] = x[(size_t)idx[m] * d + j];
+  kmeans_lloyd(x, N, d, k, cfg->iters, c, labels);
+  for (size_t i = 0; i < c.size(); ++i) centroids[i] = (int8_t)c[i];
+}
+
+void orc_kmeans_warm(const uint16_t* v, const orc_head_cfg* cfg, const int8_t* prev_centroids,
+                     float prev_grid_scale, int8_t* x_out, float* grid_scale_out,
+                     int32_t* labels, int8_t* centroids) {
+  const int N = cfg->N, d = cfg->d, k = cfg->k;
+  std::vector<int> x;
+  const float s = kmeans_features(v, N, d, x);
+  if (x_out)
+    for (size_t i = 0; i < x.size(); ++i) x_out[i] = (int8_t)x[i];
+  *grid_scale_out = s;
+
+  // The previous step's centroids, kept at the same place in value units:
+  // on the new grid c = clamp(RNE(c_prev * (s_prev / s)), -127, 127), the
+  // ratio and the product each rounded to fp32.
+  const float r = prev_grid_scale / s;
+  std::vector<int> c((size_t)k * d);
+  for (size_t i = 0; i < c.size(); ++i) {
+    const float t = std::nearbyintf((float)prev_centroids[i] * r);
+    c[i] = (int)std::min(127.0f, std::max(-127.0f, t));
+  }
+  kmeans_lloyd(x, N, d, k, cfg->iters, c, labels);
   for (size_t i = 0; i < c.size(); ++i) centroids[i] = (int8_t)c[i];
 }
 

@@ -76,6 +76,18 @@ void orc_kmeans(const uint16_t* v, const orc_head_cfg* cfg,
                 int8_t* x_out /* N*d, may be NULL */, float* grid_scale_out,
                 int32_t* labels_out, int8_t* centroids_out);
 
+/* Warm-started k-means (paper §3.2, "Unbalanced clusters cost little": each
+ * step starts from the previous step's centroids).  The previous centroids
+ * (on the grid of scale prev_grid_scale) are moved to this head's grid at the
+ * same value-space position, c = clamp(RNE(c_prev * (prev_grid_scale / s)),
+ * -127, 127) with the ratio and the product rounded to fp32, then cfg->iters
+ * Lloyd iterations run as in orc_kmeans.  With cfg->iters = 0 the outputs are
+ * the moved centroids (labels untouched).  Pinned: exact halving when the
+ * grid doubles, fixed point of a converged run, brute-force assignment. */
+void orc_kmeans_warm(const uint16_t* v, const orc_head_cfg* cfg, const int8_t* prev_centroids,
+                     float prev_grid_scale, int8_t* x_out /* may be NULL */,
+                     float* grid_scale_out, int32_t* labels_out, int8_t* centroids_out);
+
 /* Stable counting sort of labels: perm[i] = source token of permuted row i. */
 void orc_stable_argsort(const int32_t* labels, int N, int k, int32_t* perm_out);
 

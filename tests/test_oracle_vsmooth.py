@@ -142,6 +142,75 @@ def test_kmeans_brute_force_fixed_point(orc, iters):
     assert np.array_equal(lab1, np.argmin(d0, axis=1))
 
 
+def _doubled_amax_copy(vb, base=None):
+    """`base` (default vb) with one element set to exactly twice the largest
+    |vb|: when every other |element| stays below that, the feature grid scale
+    is exactly twice vb's (scaling by 2 commutes with fp32 rounding)."""
+    vf = _f(vb)
+    amax = np.abs(vf).max()
+    v2 = np.array(vb if base is None else base, copy=True)
+    assert np.abs(_f(v2)).max() < 2 * amax
+    r, c = np.unravel_index(np.argmax(np.abs(vf)), vf.shape)
+    v2[(r + 1) % vf.shape[0], c] = _bf16(np.float32(2 * amax))[()]
+    return v2
+
+
+def test_kmeans_warm_moves_centroids_to_the_new_grid(orc):
+    """Warm start: when the grid scale doubles exactly, the previous centroids
+    land on the new grid at exactly half their integer value, rounded half to
+    even (numpy rint); an unchanged grid leaves them untouched."""
+    rng = np.random.default_rng(7)
+    N, d, k = 96, 16, 6
+    vb = _bf16(rng.standard_normal((N, d)) * 2 + np.repeat(rng.standard_normal((6, d)) * 4, 16, 0))
+    _, s1, _, c1 = orc.kmeans(vb, k, 4, 5)
+    assert (np.abs(c1) % 2 == 1).any()      # odd codes exercise the tie rule
+    v2 = _doubled_amax_copy(vb)
+    _, s2, lab, c2 = orc.kmeans_warm(v2, c1, s1, 0)
+    assert s2 == 2 * s1
+    assert np.array_equal(c2, np.rint(c1.astype(np.float64) / 2).astype(np.int8))
+    assert (lab == -1).all()
+    _, s3, _, c3 = orc.kmeans_warm(vb, c1, s1, 0)
+    assert s3 == s1 and np.array_equal(c3, c1)
+
+
+@pytest.mark.parametrize("iters", [1, 3])
+def test_kmeans_warm_brute_force(orc, iters):
+    """Warm-started Lloyd: the first assignment is the brute-force argmin
+    (lowest index on ties) against the moved centroids; after the last update
+    the centroids are the rounded integer means of the last members."""
+    rng = np.random.default_rng(20 + iters)
+    N, d, k = 64, 16, 5
+    vb = _bf16(rng.standard_normal((N, d)) + np.repeat(rng.standard_normal((4, d)) * 3, 16, 0))
+    _, s1, _, c1 = orc.kmeans(vb, k, 3, 11)
+    v2 = _doubled_amax_copy(vb, _bf16(_f(vb) + rng.standard_normal((N, d)) * 0.5))
+    x2, s2, lab1, _ = orc.kmeans_warm(v2, c1, s1, 1)
+    assert s2 == 2 * s1
+    X = x2.astype(np.int64)
+    C0 = np.rint(c1.astype(np.float64) / 2).astype(np.int64)
+    assert np.array_equal(lab1, np.argmin(((X[:, None] - C0[None]) ** 2).sum(-1), axis=1))
+    _, _, lab_t, cent_t = orc.kmeans_warm(v2, c1, s1, iters)
+    _, _, lab_t1, cent_t1 = orc.kmeans_warm(v2, c1, s1, iters + 1)
+    C = cent_t.astype(np.int64)
+    assert np.array_equal(lab_t1, np.argmin(((X[:, None] - C[None]) ** 2).sum(-1), axis=1))
+    for m in range(k):
+        mem = X[lab_t1 == m]
+        want = cent_t[m] if len(mem) == 0 else np.rint(mem.sum(0) / len(mem)).astype(np.int8)
+        assert np.array_equal(cent_t1[m], want)
+
+
+def test_kmeans_warm_from_a_converged_run_is_a_fixed_point(orc):
+    """Started from the centroids of a converged run on the same values, warm
+    k-means changes nothing: one iteration returns the same labels and
+    centroids."""
+    q, k, v = synth.make_qkv(1, 1, 512, 128, 8, 44)
+    vb = v[0, 0]
+    _, s, lab, cent = orc.kmeans(vb, 8, 40, 3)
+    _, _, lab41, cent41 = orc.kmeans(vb, 8, 41, 3)
+    assert np.array_equal(lab, lab41) and np.array_equal(cent, cent41)   # converged
+    _, s_w, lab_w, cent_w = orc.kmeans_warm(vb, cent, s, 1)
+    assert s_w == s and np.array_equal(lab_w, lab) and np.array_equal(cent_w, cent)
+
+
 def test_kmeans_objective_nonincreasing_and_clusters_found(orc):
     # Lloyd on the integer grid: the rounded mean is the best integer centre per
     # coordinate, so the within-cluster sum of squares never increases.
