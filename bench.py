@@ -74,6 +74,15 @@ def attn_traffic(w):
     return ref["bytes"] * (w.B * w.H * w.N) / ref["tokens"]
 
 
+def grouping_mode(args) -> str:
+    return "reuse" if args.reuse else ("warm" if args.warm else "fresh")
+
+
+def grouping_iters(args) -> int:
+    """Lloyd iterations of a timed step: a warm start runs half as many."""
+    return max(1, args.iters // 2) if args.warm else args.iters
+
+
 def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
     """Algorithmic DRAM bytes of one V-Smooth preparation: read Q, K, V (bf16)
     once for the quantisers and V once more for the grouping features; write
@@ -98,7 +107,8 @@ def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
 
 def launches_per_step(iters: int, reuse: bool, bits: int = 8) -> int:
     """Kernels of libvca launched by one step (preparation chain + attention)."""
-    grouping = 0 if reuse else (1 + 1 + 1 + 1 + 2 * iters + 3)  # zero, amax, features, init, iters, sort
+    # zero, amax, features, init (or warm start), iterations, sort
+    grouping = 0 if reuse else (1 + 1 + 1 + 1 + 2 * iters + 3)
     # 8-bit Q/K/V passes: Q, K, V1, V reduce, zero, V2; 4-bit: zero, |Q| max,
     # |K'| max, V1, global scales, Q, K, zero, V2
     passes = 6 if bits == 8 else 9
@@ -161,16 +171,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def cpu_oracle_sample(w, rows_per_head=16, seed_rows=0):
-    """Time the CPU oracle on one head of the workload (full preparation and
-    `rows_per_head` attention rows), extrapolated to the whole workload."""
+def cpu_oracle_sample(w, rows_per_head=16, seed_rows=0, iters=10):
+    """Time the CPU oracle on one head of the workload (full preparation with a
+    fresh grouping of `iters` Lloyd iterations, and `rows_per_head` attention
+    rows), extrapolated to the whole workload."""
     import oracle
     oracle.build()
     q, k, v = synth.make_qkv(1, 1, w.N, w.d, w.clusters, w.seed)
     t0 = time.perf_counter()
     prepare, attention = ((oracle.prepare8, oracle.attention8) if w.bits == 8
                           else (oracle.prepare4, oracle.attention4))
-    p = prepare(q[0, 0], k[0, 0], v[0, 0], w.k, 10, 0, b=0, h=0, H=1)
+    p = prepare(q[0, 0], k[0, 0], v[0, 0], w.k, iters, 0, b=0, h=0, H=1)
     t_prep = time.perf_counter() - t0
     rows = np.random.default_rng(seed_rows).choice(w.N, rows_per_head, replace=False)
     t0 = time.perf_counter()
@@ -179,7 +190,8 @@ def cpu_oracle_sample(w, rows_per_head=16, seed_rows=0):
     heads = w.B * w.H
     t_step = heads * (t_prep + t_rows * w.N / rows_per_head)
     return dict(value=w.flops / t_step / 1e12, t_step_s=t_step, t_prep_head_s=t_prep,
-                t_rows_s=t_rows, sample=f"1 of {heads} heads: full V-Smooth preparation + "
+                t_rows_s=t_rows, sample=f"1 of {heads} heads: full V-Smooth preparation "
+                f"(fresh grouping, {iters} Lloyd iterations) + "
                 f"{rows_per_head} of {w.N} attention rows, extrapolated linearly per head and row")
 
 
@@ -189,7 +201,7 @@ def run_reference(args, w):
         return
     times, vals = [], []
     for i in range(args.warmup + args.steps):
-        r = cpu_oracle_sample(w, rows_per_head=8, seed_rows=i)
+        r = cpu_oracle_sample(w, rows_per_head=8, seed_rows=i, iters=args.iters)
         if i >= args.warmup:
             vals.append(r["value"])
             times.append(r["t_step_s"])
@@ -253,10 +265,20 @@ def run_gpu(args, w):
                           device=dev)
     attn_fn = vca.attention_fp8 if w.bits == 8 else vca.attention_nvfp4
 
+    # the first step groups from scratch; later steps reuse or warm-start
+    # from its result when asked to
+    mode = {"fresh": vca.PERM_FRESH, "reuse": vca.PERM_REUSE, "warm": vca.PERM_WARM}[
+        grouping_mode(args)]
+
+    def prep_args():
+        if not att_ready[0]:
+            return dict(reuse_perm=vca.PERM_FRESH)
+        return dict(reuse_perm=mode, iters=grouping_iters(args))
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        att.prepare(q, k, v, reuse_perm=args.reuse and att_ready[0])
+        att.prepare(q, k, v, **prep_args())
         if ev:
             ev[1].record(stream)
         attn_fn(att.state, shape, out)
@@ -331,7 +353,7 @@ def run_gpu(args, w):
                 cstream.wait_event(in_ready[i % 2])
                 if i >= 2:
                     cstream.wait_event(d2h_done[i % 2])           # step i-2's O was read back
-                att.prepare(b[0], b[1], b[2], stream=cstream)
+                att.prepare(b[0], b[1], b[2], stream=cstream, **prep_args())
                 attn_fn(att.state, shape, b[3], stream=cstream)
                 consumed[i % 2].record(cstream)
                 with torch.cuda.stream(d2h_stream):
@@ -381,7 +403,8 @@ def run_gpu(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3" if w.bits == 8 else "e2m1", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
-                   "iters": args.iters, "bits": w.bits, "reuse_perm": bool(args.reuse),
+                   "iters": grouping_iters(args), "bits": w.bits,
+                   "reuse_perm": bool(args.reuse), "grouping": grouping_mode(args),
                    "step": "V-Smooth preparation + fused attention",
                    "l2": "inputs (3 x %.2f GB) larger than L2; no flush" % (nbytes / 1e9),
                    "parallelism": f"independent problem per GPU x{world}"},
@@ -389,9 +412,9 @@ def run_gpu(args, w):
         f"pct_{pname}_peak": 100.0 * attn_tflops / tc_peak,
         f"pct_{pname}_nominal": 100.0 * attn_tflops / NOMINAL_TFLOPS[w.bits],
         "vsmooth_ms": statistics.mean(prep_ms),
-        "vsmooth_gbs": vsmooth_bytes(w, args.iters, args.reuse) / (statistics.mean(prep_ms) * 1e-3)
-        / 1e9,
-        "vsmooth_bytes": vsmooth_bytes(w, args.iters, args.reuse),
+        "vsmooth_gbs": vsmooth_bytes(w, grouping_iters(args), args.reuse)
+        / (statistics.mean(prep_ms) * 1e-3) / 1e9,
+        "vsmooth_bytes": vsmooth_bytes(w, grouping_iters(args), args.reuse),
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
@@ -405,13 +428,13 @@ def run_gpu(args, w):
                  "overlap": "pinned copies on a second stream: step i+1's inputs and step i's "
                             "output move during the neighbouring step's compute"}
                 if e2e_ms else None),
-        "gpu_launches": launches_per_step(args.iters, args.reuse, w.bits) * args.steps,
+        "gpu_launches": launches_per_step(grouping_iters(args), args.reuse, w.bits) * args.steps,
         "clocks": clocks.summary(),
     }
     if dist:
         dist.barrier()
     if rank == 0 and not args.no_cpu_baseline:
-        r = cpu_oracle_sample(w)
+        r = cpu_oracle_sample(w, iters=grouping_iters(args))
         line["cpu_baseline"] = {"value": r["value"], "unit": "TFLOPS", "cores": 1,
                                 "kind": "oracle", "sample": r["sample"]}
     if rank == 0:
@@ -429,10 +452,14 @@ def main():
     ap.add_argument("--workload", default="wan720p", choices=sorted(synth.CONFIGS))
     ap.add_argument("--iters", type=int, default=10)
     ap.add_argument("--reuse", action="store_true", help="reuse the cached permutation")
+    ap.add_argument("--warm", action="store_true",
+                    help="warm-start k-means from the cached centroids, half the iterations")
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
+    if args.reuse and args.warm:
+        ap.error("--reuse and --warm exclude each other")
     w = synth.CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -51,6 +51,8 @@ __device__ __forceinline__ uint64_t splitmix64_next(uint64_t& s) {
 // ---------------------------------------------------------------------------
 // state header / reuse check
 // ---------------------------------------------------------------------------
+// reuse: 0 fresh grouping, 1 cached permutation, 2 grouping warm-started from
+// the cached centroids (modes 1 and 2 need a grouping of the same problem)
 __global__ void header_kernel(uint32_t* hdr, int* status, int B, int H, int N, int d, int k,
                               int bits, int reuse) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -59,7 +61,10 @@ __global__ void header_kernel(uint32_t* hdr, int* status, int B, int H, int N, i
                        hdr[3] == (uint32_t)N && hdr[4] == (uint32_t)d && hdr[5] == (uint32_t)k &&
                        hdr[6] == (uint32_t)bits && hdr[7] == 1u;
     *status = match ? 0 : kStatNoPerm;
-    if (match) hdr[8] = 0;  // operands being rewritten
+    if (match) {
+      if (reuse == 2) hdr[7] = 0;  // permutation being recomputed
+      hdr[8] = 0;                  // operands being rewritten
+    }
     return;
   }
   hdr[0] = kStateMagic;
@@ -159,6 +164,29 @@ __global__ void kmeans_init_kernel(const int8_t* x, int8_t* cent, int32_t* sums,
       cent[((size_t)bh * k + m) * d + c] = x[((size_t)bh * N + idx[m]) * d + c];
       sums[((size_t)bh * k + m) * d + c] = 0;
     }
+  for (int m = threadIdx.x; m < k; m += blockDim.x) counts[(size_t)bh * k + m] = 0;
+}
+
+// grid BH, 128 threads: warm start (paper §3.2, "Unbalanced clusters cost
+// little": each step starts from the previous step's centroids).  The cached
+// centroids, on the grid of the cached scale s', move to this call's grid
+// s = amax / 127 at the same value-space position: c = clamp(RNE(c (s' / s)),
+// -127, 127), the ratio and the product rounded to fp32.  Runs before the
+// features kernel overwrites s'; zeroes the sums.
+__global__ void kmeans_warm_kernel(const uint32_t* amax_bits, const float* grid_scale,
+                                   int8_t* cent, int32_t* sums, int32_t* counts, int k, int d,
+                                   const int* status) {
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.x;
+  const float amax = __uint_as_float(amax_bits[bh]);
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+  const float r = __fdiv_rn(grid_scale[bh], s);
+  for (int i = threadIdx.x; i < k * d; i += blockDim.x) {
+    int8_t* c = cent + (size_t)bh * k * d + i;
+    const int t = __float2int_rn(__fmul_rn((float)*c, r));
+    *c = (int8_t)max(-127, min(127, t));
+    sums[(size_t)bh * k * d + i] = 0;
+  }
   for (int m = threadIdx.x; m < k; m += blockDim.x) counts[(size_t)bh * k + m] = 0;
 }
 
@@ -1031,8 +1059,9 @@ inline int grid_chunks(size_t work, int per_block, int cap) {
 // ---------------------------------------------------------------------------
 // host: the preparation chain
 // ---------------------------------------------------------------------------
-// Header, grouping (skipped when the cached permutation is reused) and the
-// key channel mean: the part of the chain both bit widths share.
+// Header, grouping (skipped when the cached permutation is reused; started
+// from the cached centroids when warm) and the key channel mean: the part of
+// the chain both bit widths share.
 static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   const int BH = a.B * a.H, N = a.N, nb = a.nb, k = a.k;
   const size_t per_head = (size_t)N * 128;
@@ -1046,7 +1075,7 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   int32_t* perm = reinterpret_cast<int32_t*>(S + L.perm);
 
   header_kernel<<<1, 32, 0, st>>>(hdr, status, a.B, a.H, N, 128, k, bits, a.reuse);
-  if (!a.reuse) {
+  if (a.reuse != 1) {
     uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + L.grid);
     float* gscale = reinterpret_cast<float*>(S + L.grid) + BH;
     int8_t* x = reinterpret_cast<int8_t*>(S + L.features);
@@ -1056,8 +1085,12 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
     zero_kernel<<<1, 256, 0, st>>>(amax_bits, BH);
     const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
     head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, per_head, status);
+    if (a.reuse == 2)
+      kmeans_warm_kernel<<<BH, 128, 0, st>>>(amax_bits, gscale, cent, sums, counts, k, 128,
+                                             status);
     features_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
-    kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
+    if (a.reuse == 0)
+      kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
     if (k <= 128) {
       // tensor-core Lloyd iteration (the cluster-sum product has M = 128 rows):
       // each CTA takes a run of tiles of one head, runs sized to fill whole
@@ -1148,7 +1181,7 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroupBytes / 4);
   vpass2_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, sv, rhatT, mut, mside, N, Npad, nb,
                                               ngroups, ngroups * kGroup - nb, status);
-  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse != 1);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 
@@ -1186,7 +1219,7 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroup4Bytes / 4);
   vpass2_4_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, g4, S + L.r4T, S + L.kr4s, mside, N,
                                                 Npad, nb, ngroups, ngroups * kGroup4 - nb, status);
-  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, !a.reuse);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse != 1);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 

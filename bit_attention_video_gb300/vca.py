@@ -23,6 +23,8 @@ STATUS_NAMES = {0: "VCA_OK", -1: "VCA_ERR_INVALID_ARG", -2: "VCA_ERR_UNSUPPORTED
                 -7: "VCA_ERR_STATE_MISMATCH"}
 DEFAULT_ITERS = 10
 DEFAULT_SEED = 0
+# reuse_perm modes of vsmooth_prepare (False / True map to FRESH / REUSE)
+PERM_FRESH, PERM_REUSE, PERM_WARM = 0, 1, 2
 
 
 class VcaError(RuntimeError):
@@ -199,6 +201,7 @@ def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
         labels=v(L.labels, BH * N, torch.int32, (BH, N)),
         perm=v(L.perm, BH * N, torch.int32, (BH, N)),
         centroids=v(L.centroids, BH * k_clusters * d, torch.int8, (BH, k_clusters, d)),
+        grid_scale=v(L.grid + 4 * BH, BH, torch.float32, (BH,)),   # k-means feature grid
         kbar=v(L.kbar, BH * d, torch.int16, (BH, d)),
         mu=v(L.mu, BH * nb * d, torch.int16, (BH, nb, d)),
         status=v(L.status, 1, torch.int32, (1,)),
@@ -238,9 +241,12 @@ class VCAttention:
         self.k, self.bits, self.iters, self.seed = k_clusters, bits, iters, seed
         self.state = alloc_state(B, H, N, d, k_clusters, bits, device)
 
-    def prepare(self, q, k, v, reuse_perm=False, stream=None):
-        vsmooth_prepare(q, k, v, self.k, self.state, reuse_perm, self.bits, self.iters,
-                        self.seed, stream)
+    def prepare(self, q, k, v, reuse_perm=False, stream=None, iters=None):
+        """reuse_perm: PERM_FRESH / PERM_REUSE / PERM_WARM (or False / True);
+        iters overrides the Lloyd iteration count of this call (a warm start
+        usually runs fewer)."""
+        vsmooth_prepare(q, k, v, self.k, self.state, reuse_perm, self.bits,
+                        self.iters if iters is None else iters, self.seed, stream)
 
     def attention(self, out, stream=None):
         fn = attention_fp8 if self.bits == 8 else attention_nvfp4

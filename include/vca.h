@@ -50,6 +50,10 @@ typedef enum {
 
 #define VCA_DEFAULT_ITERS 10
 #define VCA_DEFAULT_SEED 0ull
+/* reuse_perm modes of vca_vsmooth_prepare */
+#define VCA_PERM_FRESH 0
+#define VCA_PERM_REUSE 1
+#define VCA_PERM_WARM 2
 #define VCA_BLOCK_ROWS 128 /* B_v: the hardware block of the block means (paper §3.2, Eq 4) */
 
 /* Offsets (bytes from the start of the state blob) of every array the
@@ -106,10 +110,19 @@ int vca_state_layout_get(int B, int H, int N, int d, int k_clusters, int bits,
  * Appx B).  Reads q, k, v (bf16 [B,H,N,d], device) and writes every operand of
  * the attention kernels into `state` (device, state_bytes >= vca_state_bytes).
  *   k_clusters  k-means clusters per (b, h)
- *   reuse_perm  0: run k-means (iters Lloyd iterations, seeded by `seed`) and
- *               cache pi and the centroids in the blob; 1: skip grouping and
- *               reuse the cached pi (paper §3.4 "Amortized grouping
- *               schedule"); the blob must come from a call with the same
+ *   reuse_perm  VCA_PERM_FRESH (0): run k-means (iters Lloyd iterations,
+ *               seeded by `seed`) and cache pi, the centroids and the feature
+ *               grid scale in the blob;
+ *               VCA_PERM_REUSE (1): skip grouping and reuse the cached pi
+ *               (paper §3.4 "Amortized grouping schedule");
+ *               VCA_PERM_WARM (2): run iters Lloyd iterations started from
+ *               the cached centroids (paper §3.2 "Unbalanced clusters cost
+ *               little": warm-starting each step from the previous step's
+ *               centroids), moved to this call's feature grid at the same
+ *               value-space position, c = clamp(RNE(c * (s_cached / s)),
+ *               -127, 127) in fp32; `seed` is unused; the new pi, centroids
+ *               and scale replace the cached ones.
+ *               Modes 1 and 2 need a blob grouped by a call with the same
  *               B, H, N, d, k_clusters and bits, else the status word gets
  *               VCA_ERR_NO_CACHED_PERM and no operand is written.
  *   bits        8 (E4M3 path) or 4 (NVFP4 path)

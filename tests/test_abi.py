@@ -66,7 +66,8 @@ def test_prepare_rejects_bad_arguments(L):
     assert call(state=None) == -1
     assert call(v=mis) == -1
     assert call(iters=0) == -1
-    assert call(reuse=2) == -1
+    assert call(reuse=3) == -1       # 0 fresh, 1 reuse, 2 warm
+    assert call(reuse=-1) == -1
     assert call(N=0) == -1
     assert call(d=64) == -2
     assert call(bits=6) == -2

@@ -101,6 +101,55 @@ def test_reuse_permutation(orc):
         check_head8(g2, p, h, N, what=("perm",))
 
 
+@pytest.mark.parametrize("bits,B,H,N,C,kc,it0,it1", [
+    (8, 1, 2, 1000, 16, 16, 4, 2),     # ragged last block
+    (8, 2, 1, 2500, 64, 40, 3, 1),     # B > 1, several sort chunks
+    (8, 1, 1, 700, 32, 144, 2, 2),     # k > 128 (the CUDA-core assignment)
+    (4, 1, 2, 640, 16, 16, 3, 2),      # the 4-bit preparation shares the grouping
+])
+def test_warm_start_matches_oracle(orc, bits, B, H, N, C, kc, it0, it1):
+    """A fresh grouping of one step, then a warm start on the next step's
+    values: labels, permutation, centroids and feature grid scale are
+    bit-exact with the oracle's warm k-means, and so is every operand."""
+    from bit_attention_video_gb300 import vca
+    q, k, v = synth.make_qkv(B, H, N, 128, C, 21)
+    q2, k2, v2 = synth.make_qkv(B, H, N, 128, C, 22)     # the next "denoising step"
+    v2[0, 0, 3, 5] = 0x4300                              # 128.0: the grid scale changes
+    state, st, g1 = gpu_prepare(q, k, v, kc, it0, 13, bits=bits)
+    assert st == 0
+    state, st, g2 = gpu_prepare(q2, k2, v2, kc, it1, 13, bits=bits, reuse=vca.PERM_WARM,
+                                state=state)
+    assert st == 0
+    for b in range(B):
+        for h in range(H):
+            bh = b * H + h
+            _, s1, _, c1 = orc.kmeans(v[b, h], kc, it0, 13, b=b, h=h, H=H)
+            assert np.array_equal(g1["centroids"][bh], c1) and g1["grid_scale"][bh] == s1
+            _, s2, lab, cent = orc.kmeans_warm(v2[b, h], c1, s1, it1)
+            assert g2["grid_scale"][bh] == s2
+            assert np.array_equal(g2["labels"][bh], lab), f"head {bh}: labels"
+            assert np.array_equal(g2["centroids"][bh], cent), f"head {bh}: centroids"
+            perm = orc.stable_argsort(lab, kc)
+            assert np.array_equal(g2["perm"][bh], perm), f"head {bh}: perm"
+            if bits == 8:
+                p = orc.prepare8(q2[b, h], k2[b, h], v2[b, h], kc, it1, 13, perm=perm)
+                check_head8(g2, p, bh, N, what=("perm",))
+    # a reuse after the warm start keeps the warm permutation
+    state, st, g3 = gpu_prepare(q, k, v, kc, it1, 13, bits=bits, reuse=vca.PERM_REUSE,
+                                state=state)
+    assert st == 0 and np.array_equal(g3["perm"], g2["perm"])
+
+
+def test_warm_start_without_cached_grouping_is_reported(orc):
+    from bit_attention_video_gb300 import vca
+    B, H, N, kc = 1, 1, 300, 4
+    q, k, v = synth.make_qkv(B, H, N, 128, 4, 5)
+    state = vca.alloc_state(B, H, N, 128, kc, 8)
+    state.zero_()
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, state, vca.PERM_WARM, 8, 2, 0)
+    assert vca.get_status(state) == -5
+
+
 def test_reuse_without_cached_permutation_is_reported(orc):
     from bit_attention_video_gb300 import vca
     B, H, N, kc = 1, 1, 300, 4
