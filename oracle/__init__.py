@@ -106,6 +106,10 @@ def _declare(L):
     L.orc_prepare8.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.POINTER(Prep8Out)]
     L.orc_prepare4.restype = None
     L.orc_prepare4.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.POINTER(Prep4Out)]
+    L.orc_prepare8_plain.restype = None
+    L.orc_prepare8_plain.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.POINTER(Prep8Out)]
+    L.orc_prepare4_plain.restype = None
+    L.orc_prepare4_plain.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.POINTER(Prep4Out)]
     L.orc_attention_exact.restype = None
     L.orc_attention_exact.argtypes = [_P, _P, _P, C.c_int, C.c_int, _P, C.c_int, _P]
     L.orc_attention_recurrence.restype = None
@@ -254,8 +258,11 @@ def block_demean(vperm_bf16: np.ndarray, Bv: int):
     return mu, r
 
 
-def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None) -> dict:
-    """One head, inputs uint16 bf16 [N, d]. Returns a dict of numpy arrays."""
+def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=False) -> dict:
+    """One head, inputs uint16 bf16 [N, d]. Returns a dict of numpy arrays.
+    plain: a step after the grouping window (needs perm): no block demeaning."""
+    if plain and perm is None:
+        raise ValueError("the plain preparation needs the permutation")
     q, k, v = (_c(x, np.uint16) for x in (q, k, v))
     N, d = q.shape
     nb = (N + BV - 1) // BV
@@ -270,13 +277,16 @@ def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None) -> dict
     st = Prep8Out(*[_ptr(o[n]) for n, _ in Prep8Out._fields_])
     cfg = _cfg(N, d, k_clusters, iters, 8, seed, b, h, H)
     keep = _c(perm, np.int32) if perm is not None else None
-    lib().orc_prepare8(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg),
-                       _ptr(keep) if keep is not None else None, C.byref(st))
+    fn = lib().orc_prepare8_plain if plain else lib().orc_prepare8
+    fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
+       C.byref(st))
     o["N"], o["d"], o["_struct"] = N, d, st
     return o
 
 
-def prepare4(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None) -> dict:
+def prepare4(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=False) -> dict:
+    if plain and perm is None:
+        raise ValueError("the plain preparation needs the permutation")
     q, k, v = (_c(x, np.uint16) for x in (q, k, v))
     N, d = q.shape
     nb = (N + BV - 1) // BV
@@ -292,8 +302,9 @@ def prepare4(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None) -> dict
     st = Prep4Out(*[_ptr(o[n]) for n, _ in Prep4Out._fields_])
     cfg = _cfg(N, d, k_clusters, iters, 4, seed, b, h, H)
     keep = _c(perm, np.int32) if perm is not None else None
-    lib().orc_prepare4(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg),
-                       _ptr(keep) if keep is not None else None, C.byref(st))
+    fn = lib().orc_prepare4_plain if plain else lib().orc_prepare4
+    fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
+       C.byref(st))
     o["N"], o["d"], o["_struct"] = N, d, st
     return o
 

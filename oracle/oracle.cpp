@@ -389,10 +389,23 @@ void quant_rows_e4m3(const float* x, int N, int d, int Bv, uint8_t* codes, float
   }
 }
 
-}  // namespace
+// The value operand: block means and residual (Eq 4), or, on the steps after
+// the grouping window (§3.4 "Amortized grouping schedule"), the permuted values
+// themselves with every mean zero.
+void split_values(const std::vector<uint16_t>& vperm, int N, int d, int Bv, bool demean,
+                  uint16_t* mu, float* r) {
+  if (demean) {
+    orc_block_demean(vperm.data(), N, d, Bv, mu, r);
+    return;
+  }
+  const int nb = num_blocks(N, Bv);
+  std::fill(mu, mu + (size_t)nb * d, (uint16_t)0);
+  std::fill(r, r + (size_t)nb * Bv * d, 0.0f);
+  for (size_t i = 0; i < (size_t)N * d; ++i) r[i] = bf(vperm[i]);
+}
 
-void orc_prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-                  const int32_t* perm_in, orc_prep8_out* out) {
+void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
+              const int32_t* perm_in, bool demean, orc_prep8_out* out) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
@@ -410,7 +423,7 @@ void orc_prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
   // V: block demeaning (Eq 4) and per-channel E4M3 of the residual (§3.2);
   // the means are stored divided by the channel scale (Appx B).
   std::vector<float> r(Npad * d);
-  orc_block_demean(f.vperm.data(), N, d, Bv, out->mu, r.data());
+  split_values(f.vperm, N, d, Bv, demean, out->mu, r.data());
   for (int c = 0; c < d; ++c) {
     float amax = 0.0f;
     for (int i = 0; i < N; ++i) amax = std::max(amax, std::fabs(r[(size_t)i * d + c]));
@@ -425,8 +438,8 @@ void orc_prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
       out->mutilde[(size_t)j * d + c] = bf(out->mu[(size_t)j * d + c]) / out->sv[c];
 }
 
-void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-                  const int32_t* perm_in, orc_prep4_out* out) {
+void prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
+              const int32_t* perm_in, bool demean, orc_prep4_out* out) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
@@ -454,7 +467,7 @@ void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
   // V: the same block demeaning; the residual in NVFP4 with blocks of 16
   // along tokens (the PV reduction dimension); means stay unscaled (Appx B).
   std::vector<float> r(Npad * d);
-  orc_block_demean(f.vperm.data(), N, d, Bv, out->mu, r.data());
+  split_values(f.vperm, N, d, Bv, demean, out->mu, r.data());
   float ra = 0.0f;
   for (size_t i = 0; i < (size_t)N * d; ++i) ra = std::max(ra, std::fabs(r[i]));
   *out->gr = nvfp4_global_scale(ra);
@@ -463,6 +476,25 @@ void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
       size_t o = (size_t)c * Npad + tb * 16;
       nvfp4_block(&r[tb * 16 * d + c], d, *out->gr, &out->r4T[o], 1, &out->r4s[o / 16]);
     }
+}
+
+}  // namespace
+
+void orc_prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
+                  const int32_t* perm_in, orc_prep8_out* out) {
+  prepare8(q, k, v, cfg, perm_in, true, out);
+}
+void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
+                  const int32_t* perm_in, orc_prep4_out* out) {
+  prepare4(q, k, v, cfg, perm_in, true, out);
+}
+void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, const int32_t* perm, orc_prep8_out* out) {
+  prepare8(q, k, v, cfg, perm, false, out);
+}
+void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out) {
+  prepare4(q, k, v, cfg, perm, false, out);
 }
 
 // ---------------------------------------------------------------------------

@@ -125,6 +125,17 @@ typedef struct {
 void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                   const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep4_out* out);
 
+/* The same preparations for the steps after the grouping window (paper §3.4
+ * "Amortized grouping schedule": the plain low-bit kernel on the permutation
+ * the window left behind): the given permutation (required), no block
+ * demeaning, so every mean is zero and the value operand is V[pi] itself.
+ * Pinned: zero means, value codes restated with torch casts, attention
+ * equal to plain quantised attention without a mean term. */
+void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, const int32_t* perm, orc_prep8_out* out);
+void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out);
+
 /* ---------------- attention (paper §3.1 Eq 1, §3.2 Eq 6, §3.3 Eq 7) ------- */
 /* Exact softmax(QK^T/sqrt d)V in fp64 on the bf16 inputs of one head, for the
  * listed query rows.  out[nrows*d] fp64.  Pinned against numpy softmax. */

@@ -105,6 +105,22 @@ def test_attention8_is_the_recurrence_on_dequantised_operands(orc, prep8):
     assert np.all(np.abs(gotb - got) <= np.abs(got) * 2.0 ** -8)
 
 
+def test_plain_attention8_is_the_recurrence_without_means(orc, prep8):
+    """After the grouping window the value operand is V[pi] itself: attention8
+    on the plain preparation is the ExpCast recurrence on the dequantised
+    operands with every mean zero."""
+    q, k, v, p0 = prep8
+    N = 700
+    p = orc.prepare8(q, k, v, 8, 5, 99, perm=p0["perm"], plain=True)
+    qd = _e4m3_val(p["qhat"][:N]) * np.repeat(p["sq"], 128)[:N, None]
+    kd = _e4m3_val(p["khat"][:N]) * np.repeat(p["sk"], 128)[:N, None]
+    rd = _e4m3_val(p["rhatT"][:, :N]).T * p["sv"][None, :]
+    rows = np.arange(1, N, 5)
+    ref = orc.attention_recurrence(qd, kd, rd, np.zeros_like(_f(p["mu"])), 128, 1, rows)
+    _, got = orc.attention8(p, rows)
+    assert np.max(np.abs(got - ref)) < 1e-9 * np.max(np.abs(ref))
+
+
 def test_attention8_value_path_with_flat_scores(orc):
     """q = 0: every score is 0, every byte is 120 (value 256), so the output is
     the mean of the dequantised residual plus the restored block means."""

@@ -290,6 +290,42 @@ def test_reuse_permutation(orc, head):
         assert np.array_equal(p2[key], head["p"][key]), key
 
 
+def test_plain_preparation_after_the_window(orc, head):
+    """After the grouping window: the same permutation, no block demeaning.
+    Every mean is zero, the value codes are per-channel E4M3 of V[pi] itself
+    (torch casts), and the Q and K operands equal the demeaned preparation's."""
+    p, N = head["p"], head["N"]
+    pp = orc.prepare8(head["q"], head["k"], head["v"], 16, 4, 4242, perm=p["perm"], plain=True)
+    assert np.array_equal(pp["perm"], p["perm"])
+    assert np.all(pp["mu"] == 0) and np.all(pp["mutilde"] == 0)
+    vp = _f(head["v"])[p["perm"]].astype(np.float32)
+    sv = np.abs(vp).max(0).astype(np.float32) / np.float32(448)
+    assert np.array_equal(pp["sv"], sv)
+    assert np.array_equal(pp["rhatT"][:, :N], _e4m3((vp / sv).T))
+    assert np.all(pp["rhatT"][:, N:] == 0)
+    for key in ("qhat", "sq", "khat", "sk", "kbar"):
+        assert np.array_equal(pp[key], p[key]), key
+    with pytest.raises(ValueError):
+        orc.prepare8(head["q"], head["k"], head["v"], 16, 4, 4242, plain=True)
+
+
+def test_plain_nvfp4_preparation(orc):
+    N, d = 400, 128
+    q, k, v = synth.make_qkv(1, 1, N, d, 8, 556)
+    p = orc.prepare4(q[0, 0], k[0, 0], v[0, 0], 8, 3, 556)
+    pp = orc.prepare4(q[0, 0], k[0, 0], v[0, 0], 8, 3, 556, perm=p["perm"], plain=True)
+    assert np.all(pp["mu"] == 0)
+    for key in ("q4", "q4s", "gq", "k4", "k4s", "gk", "kbar"):
+        assert np.array_equal(pp[key], p[key]), key
+    vp = _f(v[0, 0])[p["perm"]]
+    assert np.float32(pp["gr"][0]) == np.float32(np.abs(vp).max().astype(np.float32)) / \
+        np.float32(2688)
+    gr = float(pp["gr"][0])
+    scale = np.repeat(_e4m3_val(pp["r4s"]), 16, 1)[:, :N] * gr
+    dq = orc.e2m1_decode(pp["r4T"][:, :N].ravel()).reshape(d, N) * scale
+    assert np.all(np.abs(dq - vp.T) <= scale + 1e-6)
+
+
 def test_nvfp4_quantizers(orc):
     N, d = 400, 128
     q, k, v = synth.make_qkv(1, 1, N, d, 8, 555)
