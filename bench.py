@@ -75,7 +75,14 @@ def attn_traffic(w):
 
 
 def grouping_mode(args) -> str:
+    if args.plain:
+        return "plain"
     return "reuse" if args.reuse else ("warm" if args.warm else "fresh")
+
+
+def groups(args) -> bool:
+    """Whether a timed step runs the k-means grouping."""
+    return grouping_mode(args) in ("fresh", "warm")
 
 
 def grouping_iters(args) -> int:
@@ -267,8 +274,8 @@ def run_gpu(args, w):
 
     # the first step groups from scratch; later steps reuse or warm-start
     # from its result when asked to
-    mode = {"fresh": vca.PERM_FRESH, "reuse": vca.PERM_REUSE, "warm": vca.PERM_WARM}[
-        grouping_mode(args)]
+    mode = {"fresh": vca.PERM_FRESH, "reuse": vca.PERM_REUSE, "warm": vca.PERM_WARM,
+            "plain": vca.PERM_PLAIN}[grouping_mode(args)]
 
     def prep_args():
         if not att_ready[0]:
@@ -404,7 +411,7 @@ def run_gpu(args, w):
         "dtype": "e4m3" if w.bits == 8 else "e2m1", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
                    "iters": grouping_iters(args), "bits": w.bits,
-                   "reuse_perm": bool(args.reuse), "grouping": grouping_mode(args),
+                   "reuse_perm": not groups(args), "grouping": grouping_mode(args),
                    "step": "V-Smooth preparation + fused attention",
                    "l2": "inputs (3 x %.2f GB) larger than L2; no flush" % (nbytes / 1e9),
                    "parallelism": f"independent problem per GPU x{world}"},
@@ -412,9 +419,9 @@ def run_gpu(args, w):
         f"pct_{pname}_peak": 100.0 * attn_tflops / tc_peak,
         f"pct_{pname}_nominal": 100.0 * attn_tflops / NOMINAL_TFLOPS[w.bits],
         "vsmooth_ms": statistics.mean(prep_ms),
-        "vsmooth_gbs": vsmooth_bytes(w, grouping_iters(args), args.reuse)
+        "vsmooth_gbs": vsmooth_bytes(w, grouping_iters(args), not groups(args))
         / (statistics.mean(prep_ms) * 1e-3) / 1e9,
-        "vsmooth_bytes": vsmooth_bytes(w, grouping_iters(args), args.reuse),
+        "vsmooth_bytes": vsmooth_bytes(w, grouping_iters(args), not groups(args)),
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
@@ -428,7 +435,8 @@ def run_gpu(args, w):
                  "overlap": "pinned copies on a second stream: step i+1's inputs and step i's "
                             "output move during the neighbouring step's compute"}
                 if e2e_ms else None),
-        "gpu_launches": launches_per_step(grouping_iters(args), args.reuse, w.bits) * args.steps,
+        "gpu_launches": launches_per_step(grouping_iters(args), not groups(args), w.bits)
+        * args.steps,
         "clocks": clocks.summary(),
     }
     if dist:
@@ -454,12 +462,14 @@ def main():
     ap.add_argument("--reuse", action="store_true", help="reuse the cached permutation")
     ap.add_argument("--warm", action="store_true",
                     help="warm-start k-means from the cached centroids, half the iterations")
+    ap.add_argument("--plain", action="store_true",
+                    help="a step after the grouping window: cached permutation, no demeaning")
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
-    if args.reuse and args.warm:
-        ap.error("--reuse and --warm exclude each other")
+    if args.reuse + args.warm + args.plain > 1:
+        ap.error("--reuse, --warm and --plain exclude each other")
     w = synth.CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

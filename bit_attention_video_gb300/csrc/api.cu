@@ -120,7 +120,8 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
   if (!q || !k || !v || !state) return VCA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)state & 255u))
     return VCA_ERR_INVALID_ARG;
-  if (reuse_perm != VCA_PERM_FRESH && reuse_perm != VCA_PERM_REUSE && reuse_perm != VCA_PERM_WARM)
+  if (reuse_perm != VCA_PERM_FRESH && reuse_perm != VCA_PERM_REUSE &&
+      reuse_perm != VCA_PERM_WARM && reuse_perm != VCA_PERM_PLAIN)
     return VCA_ERR_INVALID_ARG;
   if (iters < 1 || iters > 1000) return VCA_ERR_INVALID_ARG;
   if (state_bytes < L.total_bytes) return VCA_ERR_BUFFER_TOO_SMALL;

@@ -52,7 +52,8 @@ __device__ __forceinline__ uint64_t splitmix64_next(uint64_t& s) {
 // state header / reuse check
 // ---------------------------------------------------------------------------
 // reuse: 0 fresh grouping, 1 cached permutation, 2 grouping warm-started from
-// the cached centroids (modes 1 and 2 need a grouping of the same problem)
+// the cached centroids, 3 cached permutation without block demeaning (modes
+// 1-3 need a grouping of the same problem)
 __global__ void header_kernel(uint32_t* hdr, int* status, int B, int H, int N, int d, int k,
                               int bits, int reuse) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -780,10 +781,11 @@ __device__ __forceinline__ void gather_block(const uint16_t* v, const int32_t* p
 // grid (nb, BH), 256 threads: block mean (Eq 4) of V' = V[pi]: fp32 tree sum
 // over the 128 rows (row r + row r+64, then +32, ...; padded rows 0) / n_j,
 // rounded to bf16; and the per-block residual channel maxima.  Threads
-// 0..127 own one channel each.
+// 0..127 own one channel each.  Without demeaning (the steps after the
+// grouping window, paper §3.4) every mean is 0 and the residual is V'.
 __global__ void __launch_bounds__(256) vpass1_kernel(const uint16_t* v, const int32_t* perm,
                                                      uint16_t* mu, float* vamax, int N, int nb,
-                                                     const int* status) {
+                                                     int demean, const int* status) {
   __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
@@ -795,7 +797,7 @@ __global__ void __launch_bounds__(256) vpass1_kernel(const uint16_t* v, const in
 #pragma unroll
   for (int r = 0; r < 128; ++r) x[r] = bf16_bits_to_f32(tile[r][c]);
   const float mean = __fdiv_rn(tree128(x), (float)nj);
-  const uint16_t m16 = f32_to_bf16_bits(mean);
+  const uint16_t m16 = demean ? f32_to_bf16_bits(mean) : (uint16_t)0;
   const float mf = bf16_bits_to_f32(m16);
   float amax = 0.0f;
   for (int r = 0; r < nj; ++r) amax = fmaxf(amax, fabsf(__fsub_rn(bf16_bits_to_f32(tile[r][c]), mf)));
@@ -1075,7 +1077,7 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   int32_t* perm = reinterpret_cast<int32_t*>(S + L.perm);
 
   header_kernel<<<1, 32, 0, st>>>(hdr, status, a.B, a.H, N, 128, k, bits, a.reuse);
-  if (a.reuse != 1) {
+  if (a.reuse == 0 || a.reuse == 2) {
     uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + L.grid);
     float* gscale = reinterpret_cast<float*>(S + L.grid) + BH;
     int8_t* x = reinterpret_cast<int8_t*>(S + L.features);
@@ -1174,14 +1176,15 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   float* vamax = reinterpret_cast<float*>(S + L.vamax);
   quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
   quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
-  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, a.reuse != 3,
+                                              status);
   vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
   const int ngroups = (nb + kGroup - 1) / kGroup;
   zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroupBytes / 4, 256, 4096), 256, 0, st>>>(
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroupBytes / 4);
   vpass2_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, sv, rhatT, mut, mside, N, Npad, nb,
                                               ngroups, ngroups * kGroup - nb, status);
-  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse != 1);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse == 0 || a.reuse == 2);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 
@@ -1209,7 +1212,8 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
   head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
   k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
-  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, a.reuse != 3,
+                                              status);
   g4_kernel<<<BH, 256, 0, st>>>(amax_q, amax_k, vamax, g4, nb, status);
   quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, status);
   quant_k4_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, S + L.k4, S + L.kr4s, N, Npad,
@@ -1219,7 +1223,7 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroup4Bytes / 4);
   vpass2_4_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, g4, S + L.r4T, S + L.kr4s, mside, N,
                                                 Npad, nb, ngroups, ngroups * kGroup4 - nb, status);
-  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse != 1);
+  header_done_kernel<<<1, 32, 0, st>>>(hdr, status, a.reuse == 0 || a.reuse == 2);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 

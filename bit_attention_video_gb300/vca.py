@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "VCA_OK", -1: "VCA_ERR_INVALID_ARG", -2: "VCA_ERR_UNSUPPORTED
 DEFAULT_ITERS = 10
 DEFAULT_SEED = 0
 # reuse_perm modes of vsmooth_prepare (False / True map to FRESH / REUSE)
-PERM_FRESH, PERM_REUSE, PERM_WARM = 0, 1, 2
+PERM_FRESH, PERM_REUSE, PERM_WARM, PERM_PLAIN = 0, 1, 2, 3
 
 
 class VcaError(RuntimeError):
@@ -242,7 +242,8 @@ class VCAttention:
         self.state = alloc_state(B, H, N, d, k_clusters, bits, device)
 
     def prepare(self, q, k, v, reuse_perm=False, stream=None, iters=None):
-        """reuse_perm: PERM_FRESH / PERM_REUSE / PERM_WARM (or False / True);
+        """reuse_perm: PERM_FRESH / PERM_REUSE / PERM_WARM / PERM_PLAIN (or
+        False / True);
         iters overrides the Lloyd iteration count of this call (a warm start
         usually runs fewer)."""
         vsmooth_prepare(q, k, v, self.k, self.state, reuse_perm, self.bits,

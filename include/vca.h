@@ -54,6 +54,7 @@ typedef enum {
 #define VCA_PERM_FRESH 0
 #define VCA_PERM_REUSE 1
 #define VCA_PERM_WARM 2
+#define VCA_PERM_PLAIN 3
 #define VCA_BLOCK_ROWS 128 /* B_v: the hardware block of the block means (paper §3.2, Eq 4) */
 
 /* Offsets (bytes from the start of the state blob) of every array the
@@ -121,8 +122,13 @@ int vca_state_layout_get(int B, int H, int N, int d, int k_clusters, int bits,
  *               centroids), moved to this call's feature grid at the same
  *               value-space position, c = clamp(RNE(c * (s_cached / s)),
  *               -127, 127) in fp32; `seed` is unused; the new pi, centroids
- *               and scale replace the cached ones.
- *               Modes 1 and 2 need a blob grouped by a call with the same
+ *               and scale replace the cached ones;
+ *               VCA_PERM_PLAIN (3): a step after the grouping window (paper
+ *               §3.4: the remaining steps run the plain low-bit kernel on the
+ *               permutation the window left behind): the cached pi, no block
+ *               demeaning, so every mean is 0 and the value operand is V[pi]
+ *               quantised per channel; the attention calls are unchanged.
+ *               Modes 1-3 need a blob grouped by a call with the same
  *               B, H, N, d, k_clusters and bits, else the status word gets
  *               VCA_ERR_NO_CACHED_PERM and no operand is written.
  *   bits        8 (E4M3 path) or 4 (NVFP4 path)

@@ -66,7 +66,7 @@ def test_prepare_rejects_bad_arguments(L):
     assert call(state=None) == -1
     assert call(v=mis) == -1
     assert call(iters=0) == -1
-    assert call(reuse=3) == -1       # 0 fresh, 1 reuse, 2 warm
+    assert call(reuse=4) == -1       # 0 fresh, 1 reuse, 2 warm, 3 plain
     assert call(reuse=-1) == -1
     assert call(N=0) == -1
     assert call(d=64) == -2

@@ -60,6 +60,47 @@ def test_fp8_attention_h8_sampled_rows(orc):
         assert err <= TOL8
 
 
+@pytest.mark.parametrize("bits,B,H,N,kc", [(8, 1, 2, 1000, 16), (8, 2, 1, 300, 8),
+                                            (4, 1, 2, 1000, 16)])
+def test_plain_step_after_the_window(orc, bits, B, H, N, kc):
+    """A grouping step, then a step after the grouping window on new inputs
+    (cached permutation, no block demeaning): every operand is bit-exact with
+    the oracle's plain preparation and the attention matches the oracle."""
+    from bit_attention_video_gb300 import vca
+    from test_gpu_prep import check_head8
+    from test_gpu_nvfp4 import check_head4
+    q, k, v = synth.make_qkv(B, H, N, 128, 16, 31)
+    q2, k2, v2 = synth.make_qkv(B, H, N, 128, 16, 32)
+    att = vca.VCAttention(B, H, N, 128, k_clusters=kc, bits=bits, iters=3, seed=5)
+    att.prepare(to_dev(q), to_dev(k), to_dev(v))
+    assert att.status() == 0
+    perm = vca.state_view(att.state, (B, H, N, 128), kc, bits)["perm"].cpu().numpy()
+    out = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device="cuda")
+    att.prepare(to_dev(q2), to_dev(k2), to_dev(v2), reuse_perm=vca.PERM_PLAIN)
+    att.attention(out)
+    assert att.status() == 0
+    g = {n: t.cpu().numpy() for n, t in vca.state_view(att.state, (B, H, N, 128), kc,
+                                                         bits).items()}
+    got = to_np_u16(out)
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(H):
+            bh = b * H + h
+            prep = orc.prepare8 if bits == 8 else orc.prepare4
+            p = prep(q2[b, h], k2[b, h], v2[b, h], kc, 3, 5, perm=perm[bh], plain=True)
+            assert np.all(g["mu"][bh] == 0)
+            if bits == 8:
+                check_head8(g, p, bh, N, what=("perm",))
+                _, ref = orc.attention8(p, rows)
+                tol = TOL8
+            else:
+                check_head4(g, p, bh, N, what=("perm",))
+                _, ref = orc.attention4(p, rows)
+                tol = 1e-2
+            err = rel_l2(bf16_f64(got[b, h]), ref)
+            assert err <= tol, f"(b={b},h={h}) relative L2 {err:.3e}"
+
+
 def test_fp8_attention_rejects_mismatched_state():
     from bit_attention_video_gb300 import vca
     q, k, v = synth.make_qkv(1, 1, 300, 128, 4, 1)
