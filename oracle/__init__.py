@@ -117,6 +117,10 @@ def _declare(L):
                                            _P, C.c_int, _P]
     L.orc_attention8.restype = None
     L.orc_attention8.argtypes = [C.POINTER(Prep8Out), C.c_int, C.c_int, _P, C.c_int, _P, _P]
+    L.orc_attention8_exp.restype = None
+    L.orc_attention8_exp.argtypes = [C.POINTER(Prep8Out), C.c_int, C.c_int, _P, C.c_int, _P, _P]
+    L.orc_prepare8_naive.restype = None
+    L.orc_prepare8_naive.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), C.POINTER(Prep8Out)]
     L.orc_attention4.restype = None
     L.orc_attention4.argtypes = [C.POINTER(Prep4Out), C.c_int, C.c_int, _P, C.c_int, _P, _P]
 
@@ -258,9 +262,12 @@ def block_demean(vperm_bf16: np.ndarray, Bv: int):
     return mu, r
 
 
-def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=False) -> dict:
+def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=False,
+             naive=False) -> dict:
     """One head, inputs uint16 bf16 [N, d]. Returns a dict of numpy arrays.
-    plain: a step after the grouping window (needs perm): no block demeaning."""
+    plain: a step after the grouping window (needs perm): no block demeaning.
+    naive: the comparison preparation that smooths nothing (sequence order, no
+    key centring, no demeaning); labels stay -1."""
     if plain and perm is None:
         raise ValueError("the plain preparation needs the permutation")
     q, k, v = (_c(x, np.uint16) for x in (q, k, v))
@@ -277,9 +284,12 @@ def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=F
     st = Prep8Out(*[_ptr(o[n]) for n, _ in Prep8Out._fields_])
     cfg = _cfg(N, d, k_clusters, iters, 8, seed, b, h, H)
     keep = _c(perm, np.int32) if perm is not None else None
-    fn = lib().orc_prepare8_plain if plain else lib().orc_prepare8
-    fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
-       C.byref(st))
+    if naive:
+        lib().orc_prepare8_naive(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), C.byref(st))
+    else:
+        fn = lib().orc_prepare8_plain if plain else lib().orc_prepare8
+        fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
+           C.byref(st))
     o["N"], o["d"], o["_struct"] = N, d, st
     return o
 
@@ -333,13 +343,15 @@ def attention_recurrence(q, kp, r, mu, Bv, pmode, rows=None) -> np.ndarray:
     return out
 
 
-def attention8(prep: dict, rows=None):
-    """Returns (bf16 bits [nrows, d], fp64 values before rounding)."""
+def attention8(prep: dict, rows=None, expcast=True):
+    """Returns (bf16 bits [nrows, d], fp64 values before rounding).
+    expcast=False: the conventional exponential-then-E4M3-cast bytes."""
     N, d = prep["N"], prep["d"]
     r = _rows(rows, N)
     out = np.zeros((r.size, d), np.uint16)
     out64 = np.zeros((r.size, d), np.float64)
-    lib().orc_attention8(C.byref(prep["_struct"]), N, d, _ptr(r), r.size, _ptr(out), _ptr(out64))
+    fn = lib().orc_attention8 if expcast else lib().orc_attention8_exp
+    fn(C.byref(prep["_struct"]), N, d, _ptr(r), r.size, _ptr(out), _ptr(out64))
     return out, out64
 
 

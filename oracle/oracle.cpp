@@ -337,13 +337,17 @@ struct Front {
   std::vector<uint16_t> vperm;  // permuted values, bf16 [N*d]
 };
 
+// naive: the comparison kernel that smooths nothing (sequence order, no key
+// centring): pi is the identity and kbar is 0.
 void front_half(const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
                 const int32_t* perm_in, int32_t* labels, int8_t* centroids, float* grid_scale,
-                Front& f) {
+                Front& f, bool naive = false) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   f.perm.assign(N, 0);
-  if (perm_in) {
+  if (naive) {
+    for (int i = 0; i < N; ++i) f.perm[i] = i;
+  } else if (perm_in) {
     std::copy(perm_in, perm_in + N, f.perm.begin());
   } else {
     orc_kmeans(v, cfg, nullptr, grid_scale, labels, centroids);
@@ -352,7 +356,7 @@ void front_half(const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
   // Key channel mean: fp32 tree sum per block of the original order, the block
   // sums added in block order in fp64, divided by N, rounded to fp32 then bf16.
   f.kbar.assign(d, 0);
-  for (int c = 0; c < d; ++c) {
+  for (int c = 0; c < d && !naive; ++c) {
     double total = 0.0;
     for (int j = 0; j < nb; ++j) {
       std::vector<float> w(Bv, 0.0f);
@@ -405,11 +409,11 @@ void split_values(const std::vector<uint16_t>& vperm, int N, int d, int Bv, bool
 }
 
 void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-              const int32_t* perm_in, bool demean, orc_prep8_out* out) {
+              const int32_t* perm_in, bool demean, orc_prep8_out* out, bool naive = false) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
-  front_half(k, v, cfg, perm_in, out->labels, out->centroids, out->grid_scale, f);
+  front_half(k, v, cfg, perm_in, out->labels, out->centroids, out->grid_scale, f, naive);
   std::copy(f.perm.begin(), f.perm.end(), out->perm);
   std::copy(f.kbar.begin(), f.kbar.end(), out->kbar);
 
@@ -496,6 +500,10 @@ void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out) {
   prepare4(q, k, v, cfg, perm, false, out);
 }
+void orc_prepare8_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, orc_prep8_out* out) {
+  prepare8(q, k, v, cfg, nullptr, false, out, true);
+}
 
 // ---------------------------------------------------------------------------
 // Attention
@@ -524,6 +532,11 @@ void orc_attention_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v
   }
 }
 
+// The conventional probability byte that ExpCast replaces (§3.3): the
+// exponential, then the E4M3 cast, with the same 2^8 scale as the ExpCast
+// byte: E4M3_RNE(2^(u + 8)), u <= 0 the log2-domain score minus the maximum.
+static uint8_t exp_cast_code(double u) { return orc_e4m3_encode((float)std::exp2(u + 8.0)); }
+
 // Eq 1 with the split numerator of Eq 6, over tiles of Bv keys, in fp64.
 void orc_attention_recurrence(const double* q, const double* kp, const double* r, const double* mu,
                               int N, int d, int Bv, int pmode, const int32_t* rows, int nrows,
@@ -550,7 +563,9 @@ void orc_attention_recurrence(const double* q, const double* kp, const double* r
       std::vector<double> pv(d, 0.0);
       for (int kk = k0; kk < k1; ++kk) {
         const double u = t[kk - k0] - mnew;
-        const double p = (pmode == 0) ? std::exp2(u) : orc_e4m3_decode((uint8_t)orc_expcast_code(u));
+        const double p = pmode == 0   ? std::exp2(u)
+                         : pmode == 1 ? orc_e4m3_decode((uint8_t)orc_expcast_code(u))
+                                      : orc_e4m3_decode(exp_cast_code(u));
         rsum += p;
         for (int c = 0; c < d; ++c) pv[c] += p * r[(size_t)kk * d + c];
       }
@@ -562,8 +577,8 @@ void orc_attention_recurrence(const double* q, const double* kp, const double* r
   }
 }
 
-void orc_attention8(const orc_prep8_out* P, int N, int d, const int32_t* rows, int nrows,
-                    uint16_t* out, double* out64) {
+static void attention8(const orc_prep8_out* P, int N, int d, const int32_t* rows, int nrows,
+                       bool expcast, uint16_t* out, double* out64) {
   const int Bv = 128, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   const double inv = 1.0 / std::sqrt((double)d);
@@ -594,8 +609,10 @@ void orc_attention8(const orc_prep8_out* P, int N, int d, const int32_t* rows, i
       double rsum = 0.0;
       std::vector<double> pv(d, 0.0);
       for (int kk = k0; kk < k1; ++kk) {
-        // Eq 7: the probability byte, read as E4M3 (it carries the 2^8 scale)
-        const double w = orc_e4m3_decode((uint8_t)orc_expcast_code(t[kk - k0] - mnew));
+        // Eq 7: the probability byte, read as E4M3 (it carries the 2^8 scale);
+        // or the conventional exponential and cast
+        const double u = t[kk - k0] - mnew;
+        const double w = orc_e4m3_decode(expcast ? (uint8_t)orc_expcast_code(u) : exp_cast_code(u));
         rsum += w;
         for (int c = 0; c < d; ++c) pv[c] += w * rd[(size_t)kk * d + c];
       }
@@ -611,6 +628,15 @@ void orc_attention8(const orc_prep8_out* P, int N, int d, const int32_t* rows, i
       out[(size_t)ri * d + c] = orc_f32_to_bf16((float)o);
     }
   }
+}
+
+void orc_attention8(const orc_prep8_out* P, int N, int d, const int32_t* rows, int nrows,
+                    uint16_t* out, double* out64) {
+  attention8(P, N, d, rows, nrows, true, out, out64);
+}
+void orc_attention8_exp(const orc_prep8_out* P, int N, int d, const int32_t* rows, int nrows,
+                        uint16_t* out, double* out64) {
+  attention8(P, N, d, rows, nrows, false, out, out64);
 }
 
 void orc_attention4(const orc_prep4_out* P, int N, int d, const int32_t* rows, int nrows,

@@ -133,6 +133,15 @@ void orc_prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * equal to plain quantised attention without a mean term. */
 void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep8_out* out);
+
+/* The naive 8-bit preparation the pages compare against (§4.1 "Baselines":
+ * an 8-bit kernel that rounds each operand to the nearest code per block and
+ * smooths neither; §4.5 Table 4 "Naive FP8"): sequence order (pi = identity,
+ * no grouping: labels, centroids and grid scale untouched), no key centring
+ * (kbar = 0), no block demeaning (mu = 0); Q and K per 128-token block, V per
+ * channel, all E4M3.  Pinned: codes restated with torch casts. */
+void orc_prepare8_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const orc_head_cfg* cfg, orc_prep8_out* out);
 void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out);
 
@@ -144,8 +153,9 @@ void orc_attention_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v
 
 /* The Eq 1 / Eq 6 recurrence on generic fp64 operands, for pins:
  *   keys kp[N*d], residual values r[N*d], block means mu[nb*d] (Bv rows),
- *   pmode 0: exact exp, 1: ExpCast-FP8 bytes (Eq 7), relative to the running max
- *   over Bv-key tiles.  out[nrows*d].  With pmode 0 and r = V'-1mu^T it must
+ *   pmode 0: exact exp, 1: ExpCast-FP8 bytes (Eq 7), 2: the conventional
+ *   bytes ExpCast replaces, E4M3_RNE(2^(u + 8)) (§3.3); relative to the running
+ *   max over Bv-key tiles.  out[nrows*d].  With pmode 0 and r = V'-1mu^T it must
  *   equal exact attention (mean restoration, Eq 6). */
 void orc_attention_recurrence(const double* q, const double* kp, const double* r,
                               const double* mu, int N, int d, int Bv, int pmode,
@@ -157,6 +167,14 @@ void orc_attention_recurrence(const double* q, const double* kp, const double* r
  * in out64 if non-NULL.  Compared with the GPU by relative L2. */
 void orc_attention8(const orc_prep8_out* prep, int N, int d,
                     const int32_t* rows, int nrows, uint16_t* out, double* out64);
+
+/* The same with the conventional probability bytes, E4M3_RNE(2^(u + 8)): the
+ * exponential then the cast that ExpCast-FP8 replaces (§3.3; the "Naive FP8"
+ * kernel of §4.5 Table 4 on a naive preparation, V-Smooth without ExpCast on a
+ * V-Smooth one).  Pinned: the recurrence (pmode 2) on the dequantised
+ * operands; the recurrence's bytes against torch's exp-then-cast. */
+void orc_attention8_exp(const orc_prep8_out* prep, int N, int d,
+                        const int32_t* rows, int nrows, uint16_t* out, double* out64);
 
 /* 4-bit variant: NVFP4 operands, conventional exp, NVFP4 P, means unscaled.
  * parity unpinned beyond the exact-attention error report. */

@@ -121,6 +121,61 @@ def test_plain_attention8_is_the_recurrence_without_means(orc, prep8):
     assert np.max(np.abs(got - ref)) < 1e-9 * np.max(np.abs(ref))
 
 
+def _e4m3(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def test_recurrence_exp_then_cast_single_tile(orc, small):
+    """pmode 2 on one tile (every u relative to the row maximum): the weights
+    are torch's E4M3 cast of 2^(u + 8), and the output their weighted mean."""
+    q, k, v = (_f(x) for x in small)
+    N, d = k.shape
+    rows = np.arange(0, N, 7)
+    got = orc.attention_recurrence(q, k, v, np.zeros((1, d)), 512, 2, rows)
+    t = q[rows] @ k.T / np.sqrt(d) * np.log2(np.e)
+    u = t - t.max(1, keepdims=True)
+    w = _e4m3_val(_e4m3(np.exp2(u + 8.0)))
+    want = (w @ v) / w.sum(1, keepdims=True)
+    assert np.max(np.abs(got - want)) < 1e-9 * np.max(np.abs(want))
+
+
+def test_attention8_exp_is_the_recurrence_on_dequantised_operands(orc, prep8):
+    q, k, v, p = prep8
+    N = 700
+    qd = _e4m3_val(p["qhat"][:N]) * np.repeat(p["sq"], 128)[:N, None]
+    kd = _e4m3_val(p["khat"][:N]) * np.repeat(p["sk"], 128)[:N, None]
+    rd = _e4m3_val(p["rhatT"][:, :N]).T * p["sv"][None, :]
+    rows = np.arange(2, N, 7)
+    ref = orc.attention_recurrence(qd, kd, rd, _f(p["mu"]), 128, 2, rows)
+    _, got = orc.attention8(p, rows, expcast=False)
+    assert np.max(np.abs(got - ref)) < 1e-6 * np.max(np.abs(ref))
+    _, got_ec = orc.attention8(p, rows)
+    assert np.max(np.abs(got_ec - got)) > 0          # the two byte rules differ
+
+
+def test_naive_preparation(orc):
+    """Naive FP8: sequence order, no key centring, no demeaning; Q and K per
+    128-token block, V per channel (torch E4M3 casts of the same divisions)."""
+    N = 600
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 77)
+    p = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 2, 77, naive=True)
+    ref = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 2, 77)
+    assert np.array_equal(p["perm"], np.arange(N)) and np.all(p["labels"] == -1)
+    assert np.all(p["kbar"] == 0) and np.all(p["mu"] == 0) and np.all(p["mutilde"] == 0)
+    assert np.array_equal(p["qhat"], ref["qhat"]) and np.array_equal(p["sq"], ref["sq"])
+    kf = _f(k[0, 0]).astype(np.float32)
+    for j in range(p["sk"].size):
+        blk = kf[j * 128:(j + 1) * 128]
+        s = np.float32(np.abs(blk).max()) / np.float32(448)
+        assert p["sk"][j] == s
+        assert np.array_equal(p["khat"][j * 128:j * 128 + len(blk)], _e4m3(blk / s))
+    vf = _f(v[0, 0]).astype(np.float32)
+    sv = np.abs(vf).max(0).astype(np.float32) / np.float32(448)
+    assert np.array_equal(p["sv"], sv)
+    assert np.array_equal(p["rhatT"][:, :N], _e4m3((vf / sv).T))
+
+
 def test_attention8_value_path_with_flat_scores(orc):
     """q = 0: every score is 0, every byte is 120 (value 256), so the output is
     the mean of the dequantised residual plus the restored block means."""
