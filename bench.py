@@ -43,8 +43,8 @@ PEAK_NAME = {8: "fp8", 4: "fp4"}
 # O crosses DRAM once, so the figure scales with the token count.  It holds
 # only for the kernel source it was captured on.
 ATTN_TRAFFIC = {
-    8: dict(bytes=154.310144e6 + 67.740928e6, tokens=24 * 16384,
-            sources={"attn_fp8.cu": "fb292866b4acb3e45af602ba3c6b4bc0bab4bbae0fd6fde654eb34c66c5b23a3",
+    8: dict(bytes=154.314496e6 + 67.907584e6, tokens=24 * 16384,
+            sources={"attn_fp8.cu": "a181635ea030b3dd1f424ac9bb7abc6b327b3a062847e1ca4d24c4f722499b3f",
                      "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"}),
     4: dict(bytes=88.280320e6 + 52.350976e6, tokens=24 * 16384,
             sources={"attn_nvfp4.cu": "d6a319a3ebc46b74895063894dba3d4f453e5cbd32d3ceeea567c3fc340ac539"}),
@@ -75,9 +75,17 @@ def attn_traffic(w):
 
 
 def grouping_mode(args) -> str:
+    if args.naive:
+        return "naive"
     if args.plain:
         return "plain"
     return "reuse" if args.reuse else ("warm" if args.warm else "fresh")
+
+
+def exp_bytes(args) -> bool:
+    """The 8-bit product with the conventional exp-then-cast bytes instead of
+    ExpCast (the naive comparison kernel uses them)."""
+    return args.exp or args.naive
 
 
 def groups(args) -> bool:
@@ -270,15 +278,16 @@ def run_gpu(args, w):
     out_host = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
     att = vca.VCAttention(*shape, k_clusters=w.k, bits=w.bits, iters=args.iters, seed=0,
                           device=dev)
-    attn_fn = vca.attention_fp8 if w.bits == 8 else vca.attention_nvfp4
+    attn_fn = vca.attention_nvfp4 if w.bits == 4 else (
+        vca.attention_fp8_exp if exp_bytes(args) else vca.attention_fp8)
 
     # the first step groups from scratch; later steps reuse or warm-start
     # from its result when asked to
     mode = {"fresh": vca.PERM_FRESH, "reuse": vca.PERM_REUSE, "warm": vca.PERM_WARM,
-            "plain": vca.PERM_PLAIN}[grouping_mode(args)]
+            "plain": vca.PERM_PLAIN, "naive": vca.PERM_NAIVE}[grouping_mode(args)]
 
     def prep_args():
-        if not att_ready[0]:
+        if not att_ready[0] and mode != vca.PERM_NAIVE:
             return dict(reuse_perm=vca.PERM_FRESH)
         return dict(reuse_perm=mode, iters=grouping_iters(args))
 
@@ -412,6 +421,8 @@ def run_gpu(args, w):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
                    "iters": grouping_iters(args), "bits": w.bits,
                    "reuse_perm": not groups(args), "grouping": grouping_mode(args),
+                   "probabilities": ("E4M3(exp2)" if exp_bytes(args) else "ExpCast-FP8")
+                   if w.bits == 8 else "NVFP4(exp2)",
                    "step": "V-Smooth preparation + fused attention",
                    "l2": "inputs (3 x %.2f GB) larger than L2; no flush" % (nbytes / 1e9),
                    "parallelism": f"independent problem per GPU x{world}"},
@@ -425,8 +436,11 @@ def run_gpu(args, w):
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "traffic": attn_traffic(w),
-                     "kernel": "attn_fp8_kernel" if w.bits == 8 else "attn_nvfp4_kernel",
+                     "unit": "TFLOP/s", "frac": attn_tflops / tc_peak,
+                     # counters were taken on the ExpCast instantiation only
+                     "traffic": None if exp_bytes(args) and w.bits == 8 else attn_traffic(w),
+                     "kernel": ("attn_fp8_kernel<exp>" if exp_bytes(args) else "attn_fp8_kernel")
+                     if w.bits == 8 else "attn_nvfp4_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
                                  f"{PER_BF16[w.bits]} (nominal {pname.upper()}:BF16 ratio)"},
         "e2e": ({"value": weak_value(world, w.flops, e2e_ms), "unit": "TFLOPS",
@@ -464,12 +478,16 @@ def main():
                     help="warm-start k-means from the cached centroids, half the iterations")
     ap.add_argument("--plain", action="store_true",
                     help="a step after the grouping window: cached permutation, no demeaning")
+    ap.add_argument("--naive", action="store_true",
+                    help="the naive FP8 comparison: sequence order, no smoothing, exp then cast")
+    ap.add_argument("--exp", action="store_true",
+                    help="8-bit product with exp-then-cast bytes instead of ExpCast")
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
-    if args.reuse + args.warm + args.plain > 1:
-        ap.error("--reuse, --warm and --plain exclude each other")
+    if args.reuse + args.warm + args.plain + args.naive > 1:
+        ap.error("--reuse, --warm, --plain and --naive exclude each other")
     w = synth.CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -121,7 +121,7 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ((uintptr_t)state & 255u))
     return VCA_ERR_INVALID_ARG;
   if (reuse_perm != VCA_PERM_FRESH && reuse_perm != VCA_PERM_REUSE &&
-      reuse_perm != VCA_PERM_WARM && reuse_perm != VCA_PERM_PLAIN)
+      reuse_perm != VCA_PERM_WARM && reuse_perm != VCA_PERM_PLAIN && reuse_perm != VCA_PERM_NAIVE)
     return VCA_ERR_INVALID_ARG;
   if (iters < 1 || iters > 1000) return VCA_ERR_INVALID_ARG;
   if (state_bytes < L.total_bytes) return VCA_ERR_BUFFER_TOO_SMALL;
@@ -153,7 +153,15 @@ int vca_attention_fp8(void* state, size_t state_bytes, int B, int H, int N, int 
   vca_state_layout L;
   const int rc = attention_common(state, state_bytes, B, H, N, d, o, 8, &L);
   if (rc != VCA_OK) return rc;
-  return launch_attention_fp8((uint8_t*)state, L, B, H, N, o, (cudaStream_t)stream);
+  return launch_attention_fp8((uint8_t*)state, L, B, H, N, o, true, (cudaStream_t)stream);
+}
+
+int vca_attention_fp8_exp(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,
+                          vca_stream_t stream) {
+  vca_state_layout L;
+  const int rc = attention_common(state, state_bytes, B, H, N, d, o, 8, &L);
+  if (rc != VCA_OK) return rc;
+  return launch_attention_fp8((uint8_t*)state, L, B, H, N, o, false, (cudaStream_t)stream);
 }
 
 int vca_attention_nvfp4(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,

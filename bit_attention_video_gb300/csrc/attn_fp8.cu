@@ -47,6 +47,12 @@
 // the bank and writes the slots as bf16 hi/lo to TMEM; three BF16 K=16 MMAs
 // then add sum_g rho_g mutilde_g^T (Eq 6's mean term).
 // Epilogue: O = sV (.) A / l in bf16, original query order (Q is not permuted).
+//
+// The same kernel with kExpCast = false writes the conventional bytes that
+// ExpCast replaces, E4M3_RNE(2^((a S - M')/8 + 8)): the exponential on the
+// MUFU, then the hardware E4M3 cast.  On a naive preparation this is the
+// "Naive FP8" comparison kernel of §4.5 (Table 4); on a V-Smooth one, V-Smooth
+// without ExpCast.
 #include "common.cuh"
 #include "expcast.cuh"
 #include "prep.h"
@@ -134,6 +140,7 @@ __device__ __forceinline__ bool group_ends(int j, int nb, int gpad) {
   return j == nb - 1 || (j + gpad) % kGroup == kGroup - 1;
 }
 
+template <bool kExpCast>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmR, const Fp8Params p) {
@@ -412,7 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ExpCast bytes, four per 32-bit TMEM column (the A layout of the
       // product: byte k of column c is key 4c + k)
       uint32_t w[32];
-      if (expcast_fast_is_exact(Mn)) {
+      if constexpr (!kExpCast) {
+        // x = (a S - M')/8 + 8 (one FMA; the /8 is exact), p = 2^x <= 256
+        const float a8 = a * 0.125f, b8 = 8.0f - Mn * 0.125f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[c]), a8, b8));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), a8, b8));
+          const float p2 = ex2(fmaf(__uint_as_float(s[c + 2]), a8, b8));
+          const float p3 = ex2(fmaf(__uint_as_float(s[c + 3]), a8, b8));
+          w[c / 4] = f32x4_to_e4m3x4(p0, p1, p2, p3);
+        }
+      } else if (expcast_fast_is_exact(Mn)) {
         const float a128 = a * 0.0078125f, b128 = b * 0.0078125f;
 #pragma unroll
         for (int c = 0; c < 128; c += 4) {
@@ -516,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_attention_fp8(uint8_t* S, const vca_state_layout& L, int B, int H, int N, void* o,
-                         cudaStream_t st) {
+                         bool expcast, cudaStream_t st) {
   const int BH = B * H, nb = (N + 127) / 128, Npad = nb * 128;
   CUtensorMap tq, tk, tr;
   if (!make_tmap_2d(&tq, S + L.qhat, 1, 128, (uint64_t)BH * Npad, 128, 128, 128) ||
@@ -536,12 +554,13 @@ int launch_attention_fp8(uint8_t* S, const vca_state_layout& L, int B, int H, in
   p.gpad = p.ngroups * kGroup - nb;
   p.npairs = (nb + 1) / 2;
   p.qk_scale = (float)(8.0 * 1.4426950408889634 / sqrt(128.0));
-  if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
+  auto kernel = expcast ? attn_fp8_kernel<true> : attn_fp8_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
     return VCA_ERR_CUDA;
   const long long grid = (long long)BH * p.npairs;
   if (grid > 0x7FFFFFFF) return VCA_ERR_UNSUPPORTED;
-  attn_fp8_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tr, p);
+  kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tr, p);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 

@@ -424,6 +424,10 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// four values, RNE with saturation, byte i = value i
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float v0, float v1, float v2, float v3) {
+  return (uint32_t)f32x2_to_e4m3x2(v0, v1) | ((uint32_t)f32x2_to_e4m3x2(v2, v3) << 16);
+}
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return (uint8_t)(f32x2_to_e4m3x2(x, 0.0f) & 0xFF);
 }

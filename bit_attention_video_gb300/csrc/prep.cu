@@ -53,11 +53,12 @@ __device__ __forceinline__ uint64_t splitmix64_next(uint64_t& s) {
 // ---------------------------------------------------------------------------
 // reuse: 0 fresh grouping, 1 cached permutation, 2 grouping warm-started from
 // the cached centroids, 3 cached permutation without block demeaning (modes
-// 1-3 need a grouping of the same problem)
+// 1-3 need a grouping of the same problem), 4 the naive comparison
+// preparation (sequence order, no smoothing; leaves no grouping behind)
 __global__ void header_kernel(uint32_t* hdr, int* status, int B, int H, int N, int d, int k,
                               int bits, int reuse) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  if (reuse) {
+  if (reuse >= 1 && reuse <= 3) {
     const bool match = hdr[0] == kStateMagic && hdr[1] == (uint32_t)B && hdr[2] == (uint32_t)H &&
                        hdr[3] == (uint32_t)N && hdr[4] == (uint32_t)d && hdr[5] == (uint32_t)k &&
                        hdr[6] == (uint32_t)bits && hdr[7] == 1u;
@@ -79,6 +80,14 @@ __global__ void header_done_kernel(uint32_t* hdr, const int* status, int set_per
   if (threadIdx.x != 0 || blockIdx.x != 0 || prep_skip(status)) return;
   if (set_perm) hdr[7] = 1;
   hdr[8] = 1;
+}
+
+// perm[bh][i] = i: sequence order (the naive comparison preparation)
+__global__ void identity_perm_kernel(int32_t* perm, int N, const int* status) {
+  if (prep_skip(status)) return;
+  const size_t bh = blockIdx.y;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x)
+    perm[bh * N + i] = i;
 }
 
 __global__ void zero_kernel(uint32_t* p, size_t words) {
@@ -1146,6 +1155,13 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
                                                           status);
   }
   uint16_t* kbar = reinterpret_cast<uint16_t*>(S + L.kbar);
+  if (a.reuse == 4) {
+    // naive: sequence order and no key centring (kbar = 0)
+    identity_perm_kernel<<<dim3(grid_chunks((size_t)N, 256, 64), BH), 256, 0, st>>>(perm, N,
+                                                                                   status);
+    zero_kernel<<<1, 256, 0, st>>>(reinterpret_cast<uint32_t*>(kbar), (size_t)BH * 64);
+    return VCA_OK;
+  }
   float* ksum = reinterpret_cast<float*>(S + L.ksum);
   key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
   key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
@@ -1176,8 +1192,8 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   float* vamax = reinterpret_cast<float*>(S + L.vamax);
   quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
   quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
-  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, a.reuse != 3,
-                                              status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
+                                              a.reuse != 3 && a.reuse != 4, status);
   vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
   const int ngroups = (nb + kGroup - 1) / kGroup;
   zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroupBytes / 4, 256, 4096), 256, 0, st>>>(
@@ -1212,8 +1228,8 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
   head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
   k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
-  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb, a.reuse != 3,
-                                              status);
+  vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
+                                              a.reuse != 3 && a.reuse != 4, status);
   g4_kernel<<<BH, 256, 0, st>>>(amax_q, amax_k, vamax, g4, nb, status);
   quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, status);
   quant_k4_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, S + L.k4, S + L.kr4s, N, Npad,

@@ -41,8 +41,9 @@ struct PrepArgs {
 
 int launch_prepare8(const PrepArgs& a, cudaStream_t st);
 int launch_prepare4(const PrepArgs& a, cudaStream_t st);
+// expcast = false: the conventional exponential-then-E4M3 bytes
 int launch_attention_fp8(uint8_t* state, const vca_state_layout& L, int B, int H, int N, void* o,
-                         cudaStream_t st);
+                         bool expcast, cudaStream_t st);
 int launch_attention_nvfp4(uint8_t* state, const vca_state_layout& L, int B, int H, int N,
                            void* o, cudaStream_t st);
 int launch_attention_bf16(const void* q, const void* k, const void* v, int B, int H, int N,

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "VCA_OK", -1: "VCA_ERR_INVALID_ARG", -2: "VCA_ERR_UNSUPPORTED
 DEFAULT_ITERS = 10
 DEFAULT_SEED = 0
 # reuse_perm modes of vsmooth_prepare (False / True map to FRESH / REUSE)
-PERM_FRESH, PERM_REUSE, PERM_WARM, PERM_PLAIN = 0, 1, 2, 3
+PERM_FRESH, PERM_REUSE, PERM_WARM, PERM_PLAIN, PERM_NAIVE = 0, 1, 2, 3, 4
 
 
 class VcaError(RuntimeError):
@@ -54,7 +54,7 @@ def lib():
         L.vca_state_layout_get.argtypes = [I] * 6 + [C.POINTER(StateLayout)]
         L.vca_vsmooth_prepare.restype = I
         L.vca_vsmooth_prepare.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, P, S, P]
-        for fn in ("vca_attention_fp8", "vca_attention_nvfp4"):
+        for fn in ("vca_attention_fp8", "vca_attention_fp8_exp", "vca_attention_nvfp4"):
             getattr(L, fn).restype = I
             getattr(L, fn).argtypes = [P, S, I, I, I, I, P, P]
         L.vca_attention_bf16_ref.restype = I
@@ -123,6 +123,14 @@ def vsmooth_prepare(q, k, v, k_clusters, state, reuse_perm=False, bits=8,
 def attention_fp8(state, shape, out, stream=None):
     B, H, N, d = shape
     _check("vca_attention_fp8", lib().vca_attention_fp8(
+        _dev(state, torch.uint8), state.numel(), B, H, N, d, _dev(out, torch.bfloat16),
+        _stream(stream)))
+
+
+def attention_fp8_exp(state, shape, out, stream=None):
+    """The FP8 product with the conventional exp-then-E4M3 probability bytes."""
+    B, H, N, d = shape
+    _check("vca_attention_fp8_exp", lib().vca_attention_fp8_exp(
         _dev(state, torch.uint8), state.numel(), B, H, N, d, _dev(out, torch.bfloat16),
         _stream(stream)))
 

@@ -55,6 +55,7 @@ typedef enum {
 #define VCA_PERM_REUSE 1
 #define VCA_PERM_WARM 2
 #define VCA_PERM_PLAIN 3
+#define VCA_PERM_NAIVE 4
 #define VCA_BLOCK_ROWS 128 /* B_v: the hardware block of the block means (paper §3.2, Eq 4) */
 
 /* Offsets (bytes from the start of the state blob) of every array the
@@ -127,7 +128,12 @@ int vca_state_layout_get(int B, int H, int N, int d, int k_clusters, int bits,
  *               §3.4: the remaining steps run the plain low-bit kernel on the
  *               permutation the window left behind): the cached pi, no block
  *               demeaning, so every mean is 0 and the value operand is V[pi]
- *               quantised per channel; the attention calls are unchanged.
+ *               quantised per channel; the attention calls are unchanged;
+ *               VCA_PERM_NAIVE (4): the naive comparison preparation (paper
+ *               §4.1 "Baselines", §4.5 Table 4 "Naive FP8"): sequence order
+ *               (pi = identity, no grouping), no key centring, no block
+ *               demeaning; Q and K per block and V per channel as usual.  It
+ *               leaves no grouping behind for modes 1-3.
  *               Modes 1-3 need a blob grouped by a call with the same
  *               B, H, N, d, k_clusters and bits, else the status word gets
  *               VCA_ERR_NO_CACHED_PERM and no operand is written.
@@ -148,6 +154,16 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
  * Writes o (bf16 [B,H,N,d], device) in the original query order. */
 int vca_attention_fp8(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,
                       vca_stream_t stream);
+
+/* The same product with the conventional probability bytes that ExpCast-FP8
+ * replaces (paper §3.3): E4M3_RNE(2^(u + 8)) from the fp32 exponential (MUFU)
+ * and the hardware E4M3 cast, u the log2-domain score minus the running row
+ * maximum.  On a VCA_PERM_NAIVE preparation this is the "Naive FP8" kernel the
+ * pages compare against (§4.5 Table 4); on a V-Smooth preparation it is
+ * V-Smooth without ExpCast.  Same arguments, layout and errors as
+ * vca_attention_fp8. */
+int vca_attention_fp8_exp(void* state, size_t state_bytes, int B, int H, int N, int d, void* o,
+                          vca_stream_t stream);
 
 /* 4-bit variant (paper §4.1 "Implementation", Appx A, Appx B): NVFP4 Q, K'
  * and residual with E4M3 scales per 16 elements along each product's

@@ -66,7 +66,7 @@ def test_prepare_rejects_bad_arguments(L):
     assert call(state=None) == -1
     assert call(v=mis) == -1
     assert call(iters=0) == -1
-    assert call(reuse=4) == -1       # 0 fresh, 1 reuse, 2 warm, 3 plain
+    assert call(reuse=5) == -1       # 0 fresh, 1 reuse, 2 warm, 3 plain, 4 naive
     assert call(reuse=-1) == -1
     assert call(N=0) == -1
     assert call(d=64) == -2
@@ -81,6 +81,8 @@ def test_attention_rejects_bad_arguments(L):
     nb = L.vca_state_bytes(1, 2, 300, 128, 1, 8)
     assert L.vca_attention_fp8(None, nb, 1, 2, 300, 128, fake, None) == -1
     assert L.vca_attention_fp8(fake, nb, 1, 2, 300, 128, None, None) == -1
+    assert L.vca_attention_fp8_exp(fake, nb, 1, 2, 300, 128, None, None) == -1
+    assert L.vca_attention_fp8_exp(fake, nb, 1, 2, 300, 64, fake, None) == -2
     assert L.vca_attention_fp8(fake, nb, 1, 2, 300, 64, fake, None) == -2
     assert L.vca_attention_fp8(fake, 1024, 1, 2, 300, 128, fake, None) == -4
     assert L.vca_attention_fp8(C.c_void_p((1 << 20) + 64), nb, 1, 2, 300, 128, fake, None) == -1

@@ -101,6 +101,49 @@ def test_plain_step_after_the_window(orc, bits, B, H, N, kc):
             assert err <= tol, f"(b={b},h={h}) relative L2 {err:.3e}"
 
 
+@pytest.mark.parametrize("B,H,N,kc", [(1, 2, 1000, 16), (2, 1, 129, 4)])
+def test_naive_fp8_and_vsmooth_without_expcast(orc, B, H, N, kc):
+    """The comparison kernels of the pages: the naive preparation (sequence
+    order, no smoothing) is bit-exact with the oracle's, and the conventional
+    exp-then-cast product matches the oracle on it ("Naive FP8") and on a
+    V-Smooth preparation (V-Smooth without ExpCast); the ExpCast product runs
+    on the naive preparation too."""
+    from bit_attention_video_gb300 import vca
+    from test_gpu_prep import check_head8
+    q, k, v = synth.make_qkv(B, H, N, 128, 16, 41)
+    shape = (B, H, N, 128)
+    rows = np.arange(N)
+    st_naive = vca.alloc_state(*shape, kc, 8)
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, st_naive, vca.PERM_NAIVE, 8, 3, 5)
+    st_vs = vca.alloc_state(*shape, kc, 8)
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, st_vs, vca.PERM_FRESH, 8, 3, 5)
+    outs = {}
+    for name, st, fn in (("naive_exp", st_naive, vca.attention_fp8_exp),
+                         ("naive_ec", st_naive, vca.attention_fp8),
+                         ("vs_exp", st_vs, vca.attention_fp8_exp)):
+        o = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        fn(st, shape, o)
+        outs[name] = to_np_u16(o)
+    assert vca.get_status(st_naive) == 0 and vca.get_status(st_vs) == 0
+    g = {n: t.cpu().numpy() for n, t in vca.state_view(st_naive, shape, kc, 8).items()}
+    gv = vca.state_view(st_vs, shape, kc, 8)
+    for b in range(B):
+        for h in range(H):
+            bh = b * H + h
+            pn = orc.prepare8(q[b, h], k[b, h], v[b, h], kc, 3, 5, naive=True)
+            check_head8(g, pn, bh, N, what=("perm",))
+            pv = orc.prepare8(q[b, h], k[b, h], v[b, h], kc, 3, 5, b=b, h=h, H=H)
+            assert np.array_equal(gv["perm"][bh].cpu().numpy(), pv["perm"])
+            for name, prep, ec in (("naive_exp", pn, False), ("naive_ec", pn, True),
+                                   ("vs_exp", pv, False)):
+                _, ref = orc.attention8(prep, rows, expcast=ec)
+                err = rel_l2(bf16_f64(outs[name][b, h]), ref)
+                assert err <= TOL8, f"{name} (b={b},h={h}) relative L2 {err:.3e}"
+    # the naive preparation leaves no grouping to reuse
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, st_naive, vca.PERM_REUSE, 8, 3, 5)
+    assert vca.get_status(st_naive) == -5
+
+
 def test_fp8_attention_rejects_mismatched_state():
     from bit_attention_video_gb300 import vca
     q, k, v = synth.make_qkv(1, 1, 300, 128, 4, 1)
