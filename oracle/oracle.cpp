@@ -308,6 +308,25 @@ void orc_stable_argsort(const int32_t* labels, int N, int k, int32_t* perm) {
   for (int t = 0; t < N; ++t) perm[start[labels[t]]++] = t;
 }
 
+void orc_hadamard128(const float* x, float* y) {
+  // The normalised Sylvester-Hadamard transform y = x H / sqrt(128), H[i][j] =
+  // (-1)^popcount(i & j), as the fast transform: butterflies on pairs
+  // (i, i + s) with i & s = 0 for s = 1, 2, ..., 64 in that order, each
+  // (a, b) -> (a + b, a - b) in fp32, then one fp32 multiply by the fp32
+  // value of 1/sqrt(128).
+  float t[128];
+  for (int i = 0; i < 128; ++i) t[i] = x[i];
+  for (int s = 1; s < 128; s <<= 1)
+    for (int i = 0; i < 128; ++i)
+      if ((i & s) == 0) {
+        const float a = t[i], b = t[i + s];
+        t[i] = a + b;
+        t[i + s] = a - b;
+      }
+  const float scale = (float)(1.0 / std::sqrt(128.0));
+  for (int i = 0; i < 128; ++i) y[i] = t[i] * scale;
+}
+
 void orc_block_demean(const uint16_t* vperm, int N, int d, int Bv, uint16_t* mu, float* r) {
   const int nb = num_blocks(N, Bv);
   for (int j = 0; j < nb; ++j) {
@@ -408,8 +427,15 @@ void split_values(const std::vector<uint16_t>& vperm, int N, int d, int Bv, bool
   for (size_t i = 0; i < (size_t)N * d; ++i) r[i] = bf(vperm[i]);
 }
 
+// The QK Hadamard rotation of every row of x [rows*128] in place (Appx B: the Q
+// and K kernels fuse it before quantising), as hadamard128 below.
+void rotate_rows(float* x, size_t rows) {
+  for (size_t i = 0; i < rows; ++i) orc_hadamard128(x + i * 128, x + i * 128);
+}
+
 void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-              const int32_t* perm_in, bool demean, orc_prep8_out* out, bool naive = false) {
+              const int32_t* perm_in, bool demean, orc_prep8_out* out, bool naive = false,
+              bool hadamard = false) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
@@ -420,6 +446,10 @@ void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc
   // Q: per-block E4M3, Q keeps its order (Eq 3).
   std::vector<float> qf(Npad * d, 0.0f);
   for (size_t i = 0; i < (size_t)N * d; ++i) qf[i] = bf(q[i]);
+  if (hadamard) {
+    rotate_rows(qf.data(), N);
+    rotate_rows(f.kp.data(), N);
+  }
   quant_rows_e4m3(qf.data(), N, d, Bv, out->qhat, out->sq);
   // K': per-block E4M3 of the permuted, centred keys.
   quant_rows_e4m3(f.kp.data(), N, d, Bv, out->khat, out->sk);
@@ -443,7 +473,7 @@ void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc
 }
 
 void prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-              const int32_t* perm_in, bool demean, orc_prep4_out* out) {
+              const int32_t* perm_in, bool demean, orc_prep4_out* out, bool hadamard = false) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
@@ -455,6 +485,10 @@ void prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc
   // reduction dimension) and one global scale per head.
   std::vector<float> qf(Npad * d, 0.0f);
   for (size_t i = 0; i < (size_t)N * d; ++i) qf[i] = bf(q[i]);
+  if (hadamard) {
+    rotate_rows(qf.data(), N);
+    rotate_rows(f.kp.data(), N);
+  }
   float qa = 0.0f, ka = 0.0f;
   for (size_t i = 0; i < (size_t)N * d; ++i) {
     qa = std::max(qa, std::fabs(qf[i]));
@@ -499,6 +533,14 @@ void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out) {
   prepare4(q, k, v, cfg, perm, false, out);
+}
+void orc_prepare8_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep8_out* out) {
+  prepare8(q, k, v, cfg, perm_in, true, out, false, true);
+}
+void orc_prepare4_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep4_out* out) {
+  prepare4(q, k, v, cfg, perm_in, true, out, true);
 }
 void orc_prepare8_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, orc_prep8_out* out) {

@@ -88,6 +88,14 @@ void orc_kmeans_warm(const uint16_t* v, const orc_head_cfg* cfg, const int8_t* p
                      float prev_grid_scale, int8_t* x_out /* may be NULL */,
                      float* grid_scale_out, int32_t* labels_out, int8_t* centroids_out);
 
+/* The QK Hadamard rotation (paper Appx B; §4.1 "Baselines", the fused QK
+ * Hadamard transform): y = x H / sqrt(128) for one 128-channel row, H the
+ * Sylvester-Hadamard matrix, computed as the fast transform (butterflies with
+ * stride 1, 2, ..., 64 in fp32, then an fp32 multiply by fp32(1/sqrt(128))).
+ * y may alias x.  Pinned: scipy's Hadamard matrix in fp64, exact integer
+ * inputs, orthogonality (QK^T unchanged). */
+void orc_hadamard128(const float* x, float* y);
+
 /* Stable counting sort of labels: perm[i] = source token of permuted row i. */
 void orc_stable_argsort(const int32_t* labels, int N, int k, int32_t* perm_out);
 
@@ -142,6 +150,17 @@ void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * channel, all E4M3.  Pinned: codes restated with torch casts. */
 void orc_prepare8_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, orc_prep8_out* out);
+
+/* The preparations with the QK Hadamard rotation fused into the Q and K
+ * quantisers (paper Appx B: Q fuses the rotation and quantisation; K fuses the
+ * gather, the rotation, the mean subtraction and quantisation): every row of
+ * Q and of K' = K[pi] - kbar is rotated by orc_hadamard128 before its scale
+ * and codes are taken.  QK^T is unchanged in exact arithmetic; V is untouched.
+ * Pinned: the codes restated from the rotated rows with torch casts. */
+void orc_prepare8_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep8_out* out);
+void orc_prepare4_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep4_out* out);
 void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out);
 
