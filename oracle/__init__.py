@@ -119,6 +119,12 @@ def _declare(L):
     L.orc_attention8.argtypes = [C.POINTER(Prep8Out), C.c_int, C.c_int, _P, C.c_int, _P, _P]
     L.orc_attention8_exp.restype = None
     L.orc_attention8_exp.argtypes = [C.POINTER(Prep8Out), C.c_int, C.c_int, _P, C.c_int, _P, _P]
+    L.orc_prepare8_ex.restype = None
+    L.orc_prepare8_ex.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.c_uint,
+                                  C.POINTER(Prep8Out)]
+    L.orc_prepare4_ex.restype = None
+    L.orc_prepare4_ex.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.c_uint,
+                                  C.POINTER(Prep4Out)]
     L.orc_prepare8_hadamard.restype = None
     L.orc_prepare8_hadamard.argtypes = [_P, _P, _P, C.POINTER(HeadCfg), _P, C.POINTER(Prep8Out)]
     L.orc_prepare4_hadamard.restype = None
@@ -268,6 +274,11 @@ def block_demean(vperm_bf16: np.ndarray, Bv: int):
     return mu, r
 
 
+def _opts(plain, naive, hadamard) -> int:
+    """Option bits of orc_prepare8_ex / orc_prepare4_ex."""
+    return (1 if plain else 0) | (2 if naive else 0) | (4 if hadamard else 0)
+
+
 def hadamard128(x: np.ndarray) -> np.ndarray:
     """The QK Hadamard rotation of each 128-channel row of x (fp32)."""
     x = _c(x, np.float32).reshape(-1, 128)
@@ -299,21 +310,15 @@ def prepare8(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=F
     st = Prep8Out(*[_ptr(o[n]) for n, _ in Prep8Out._fields_])
     cfg = _cfg(N, d, k_clusters, iters, 8, seed, b, h, H)
     keep = _c(perm, np.int32) if perm is not None else None
-    if naive:
-        lib().orc_prepare8_naive(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), C.byref(st))
-    else:
-        if hadamard and plain:
-            raise ValueError("the Hadamard option goes with the demeaned preparation")
-        fn = (lib().orc_prepare8_plain if plain else
-              lib().orc_prepare8_hadamard if hadamard else lib().orc_prepare8)
-        fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
-           C.byref(st))
+    lib().orc_prepare8_ex(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg),
+                          _ptr(keep) if keep is not None else None,
+                          _opts(plain, naive, hadamard), C.byref(st))
     o["N"], o["d"], o["_struct"] = N, d, st
     return o
 
 
 def prepare4(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=False,
-             hadamard=False) -> dict:
+             naive=False, hadamard=False) -> dict:
     if plain and perm is None:
         raise ValueError("the plain preparation needs the permutation")
     q, k, v = (_c(x, np.uint16) for x in (q, k, v))
@@ -331,12 +336,9 @@ def prepare4(q, k, v, k_clusters, iters, seed, b=0, h=0, H=1, perm=None, plain=F
     st = Prep4Out(*[_ptr(o[n]) for n, _ in Prep4Out._fields_])
     cfg = _cfg(N, d, k_clusters, iters, 4, seed, b, h, H)
     keep = _c(perm, np.int32) if perm is not None else None
-    if hadamard and plain:
-        raise ValueError("the Hadamard option goes with the demeaned preparation")
-    fn = (lib().orc_prepare4_plain if plain else
-          lib().orc_prepare4_hadamard if hadamard else lib().orc_prepare4)
-    fn(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg), _ptr(keep) if keep is not None else None,
-       C.byref(st))
+    lib().orc_prepare4_ex(_ptr(q), _ptr(k), _ptr(v), C.byref(cfg),
+                          _ptr(keep) if keep is not None else None,
+                          _opts(plain, naive, hadamard), C.byref(st))
     o["N"], o["d"], o["_struct"] = N, d, st
     return o
 

@@ -473,11 +473,12 @@ void prepare8(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc
 }
 
 void prepare4(const uint16_t* q, const uint16_t* k, const uint16_t* v, const orc_head_cfg* cfg,
-              const int32_t* perm_in, bool demean, orc_prep4_out* out, bool hadamard = false) {
+              const int32_t* perm_in, bool demean, orc_prep4_out* out, bool hadamard = false,
+              bool naive = false) {
   const int N = cfg->N, d = cfg->d, Bv = cfg->Bv, nb = num_blocks(N, Bv);
   const size_t Npad = (size_t)nb * Bv;
   Front f;
-  front_half(k, v, cfg, perm_in, out->labels, out->centroids, out->grid_scale, f);
+  front_half(k, v, cfg, perm_in, out->labels, out->centroids, out->grid_scale, f, naive);
   std::copy(f.perm.begin(), f.perm.end(), out->perm);
   std::copy(f.kbar.begin(), f.kbar.end(), out->kbar);
 
@@ -533,6 +534,18 @@ void orc_prepare8_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 void orc_prepare4_plain(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const orc_head_cfg* cfg, const int32_t* perm, orc_prep4_out* out) {
   prepare4(q, k, v, cfg, perm, false, out);
+}
+void orc_prepare8_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const orc_head_cfg* cfg, const int32_t* perm_in, unsigned opts,
+                     orc_prep8_out* out) {
+  prepare8(q, k, v, cfg, perm_in, (opts & (ORC_PLAIN | ORC_NAIVE)) == 0, out,
+           (opts & ORC_NAIVE) != 0, (opts & ORC_HADAMARD) != 0);
+}
+void orc_prepare4_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const orc_head_cfg* cfg, const int32_t* perm_in, unsigned opts,
+                     orc_prep4_out* out) {
+  prepare4(q, k, v, cfg, perm_in, (opts & (ORC_PLAIN | ORC_NAIVE)) == 0, out,
+           (opts & ORC_HADAMARD) != 0, (opts & ORC_NAIVE) != 0);
 }
 void orc_prepare8_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                            const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep8_out* out) {

@@ -157,6 +157,18 @@ void orc_prepare8_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * Q and of K' = K[pi] - kbar is rotated by orc_hadamard128 before its scale
  * and codes are taken.  QK^T is unchanged in exact arithmetic; V is untouched.
  * Pinned: the codes restated from the rotated rows with torch casts. */
+/* Every preparation above through one call: opts = ORC_PLAIN (no demeaning,
+ * needs perm_in), ORC_NAIVE (sequence order, no smoothing; perm_in unused),
+ * ORC_HADAMARD (the QK rotation), combinable. */
+#define ORC_PLAIN 1u
+#define ORC_NAIVE 2u
+#define ORC_HADAMARD 4u
+void orc_prepare8_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const orc_head_cfg* cfg, const int32_t* perm_in, unsigned opts,
+                     orc_prep8_out* out);
+void orc_prepare4_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const orc_head_cfg* cfg, const int32_t* perm_in, unsigned opts,
+                     orc_prep4_out* out);
 void orc_prepare8_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                            const orc_head_cfg* cfg, const int32_t* perm_in, orc_prep8_out* out);
 void orc_prepare4_hadamard(const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -81,3 +81,21 @@ def test_rotated_preparation4(orc):
         assert np.array_equal(p[key], ref[key]), key
     qr = orc.hadamard128(_f(q[0, 0]).astype(np.float32))
     assert np.float32(p["gq"][0]) == np.float32(np.abs(qr).max()) / np.float32(2688)
+
+
+def test_naive_with_rotation(orc):
+    """The pages' "8-bit FlashAttention-4 + QK Hadamard" baseline: the naive
+    preparation with the rotation, K rotated in sequence order without
+    centring."""
+    N = 260
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 63)
+    p = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 2, 63, naive=True, hadamard=True)
+    ph = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 2, 63, hadamard=True)
+    pn = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 2, 63, naive=True)
+    assert np.array_equal(p["qhat"], ph["qhat"]) and np.array_equal(p["rhatT"], pn["rhatT"])
+    kr = orc.hadamard128(_f(k[0, 0]).astype(np.float32))
+    for j in range(p["sk"].size):
+        blk = kr[j * 128:(j + 1) * 128]
+        s = np.float32(np.abs(blk).max()) / np.float32(448)
+        assert p["sk"][j] == s
+        assert np.array_equal(p["khat"][j * 128:j * 128 + len(blk)], _e4m3(blk / s))
