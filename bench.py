@@ -277,7 +277,7 @@ def run_gpu(args, w):
     out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     out_host = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
     att = vca.VCAttention(*shape, k_clusters=w.k, bits=w.bits, iters=args.iters, seed=0,
-                          device=dev)
+                          device=dev, qk_hadamard=args.qk_hadamard)
     attn_fn = vca.attention_nvfp4 if w.bits == 4 else (
         vca.attention_fp8_exp if exp_bytes(args) else vca.attention_fp8)
 
@@ -421,6 +421,7 @@ def run_gpu(args, w):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
                    "iters": grouping_iters(args), "bits": w.bits,
                    "reuse_perm": not groups(args), "grouping": grouping_mode(args),
+                   "qk_hadamard": bool(args.qk_hadamard),
                    "probabilities": ("E4M3(exp2)" if exp_bytes(args) else "ExpCast-FP8")
                    if w.bits == 8 else "NVFP4(exp2)",
                    "step": "V-Smooth preparation + fused attention",
@@ -480,6 +481,8 @@ def main():
                     help="a step after the grouping window: cached permutation, no demeaning")
     ap.add_argument("--naive", action="store_true",
                     help="the naive FP8 comparison: sequence order, no smoothing, exp then cast")
+    ap.add_argument("--qk-hadamard", action="store_true",
+                    help="fuse the QK Hadamard rotation into the Q and K quantisers")
     ap.add_argument("--exp", action="store_true",
                     help="8-bit product with exp-then-cast bytes instead of ExpCast")
     ap.add_argument("--skip-bf16", action="store_true")

@@ -114,6 +114,14 @@ int vca_state_layout_get(int B, int H, int N, int d, int k_clusters, int bits,
 int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int H, int N, int d,
                         int k_clusters, int reuse_perm, int bits, int iters, uint64_t seed,
                         void* state, size_t state_bytes, vca_stream_t stream) {
+  return vca_vsmooth_prepare_ex(q, k, v, B, H, N, d, k_clusters, reuse_perm, bits, iters, seed,
+                                0u, state, state_bytes, stream);
+}
+
+int vca_vsmooth_prepare_ex(const void* q, const void* k, const void* v, int B, int H, int N,
+                           int d, int k_clusters, int reuse_perm, int bits, int iters,
+                           uint64_t seed, unsigned flags, void* state, size_t state_bytes,
+                           vca_stream_t stream) {
   vca_state_layout L;
   const int rc = compute_layout(B, H, N, d, k_clusters, bits, &L);
   if (rc != VCA_OK) return rc;
@@ -124,6 +132,7 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
       reuse_perm != VCA_PERM_WARM && reuse_perm != VCA_PERM_PLAIN && reuse_perm != VCA_PERM_NAIVE)
     return VCA_ERR_INVALID_ARG;
   if (iters < 1 || iters > 1000) return VCA_ERR_INVALID_ARG;
+  if (flags & ~VCA_PREP_QK_HADAMARD) return VCA_ERR_INVALID_ARG;
   if (state_bytes < L.total_bytes) return VCA_ERR_BUFFER_TOO_SMALL;
   PrepArgs a;
   a.q = (const uint16_t*)q;
@@ -131,6 +140,7 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
   a.v = (const uint16_t*)v;
   a.B = B; a.H = H; a.N = N; a.nb = (N + 127) / 128; a.Npad = a.nb * 128;
   a.k = k_clusters; a.iters = iters; a.reuse = reuse_perm; a.seed = seed;
+  a.flags = flags;
   a.state = (uint8_t*)state;
   a.L = L;
   return bits == 8 ? launch_prepare8(a, (cudaStream_t)stream)

@@ -678,6 +678,29 @@ __device__ __forceinline__ void load64(const uint16_t* src, float (&f)[64]) {
     }
   }
 }
+// The QK Hadamard rotation of one 128-channel row held by a lane pair (lane
+// parity h holds channels 64h .. 64h+63): the fast transform, butterflies
+// (a, b) -> (a + b, a - b) on channels (i, i + s), i & s = 0, for s = 1 .. 32
+// inside a lane and s = 64 across the pair (the even lane keeps a + b, the odd
+// one a - b), then one multiply by fp32(1/sqrt(128)).  The whole warp calls it.
+__device__ __forceinline__ void hadamard128_pair(float (&f)[64], int h) {
+#pragma unroll
+  for (int s = 1; s < 64; s <<= 1)
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if ((i & s) == 0) {
+        const float a = f[i], b = f[i + s];
+        f[i] = __fadd_rn(a, b);
+        f[i + s] = __fsub_rn(a, b);
+      }
+  constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;  // fp32(1/sqrt(128))
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const float o = __shfl_xor_sync(0xffffffffu, f[i], 1);
+    f[i] = __fmul_rn(h == 0 ? __fadd_rn(f[i], o) : __fsub_rn(o, f[i]), kInvSqrt128);
+  }
+}
+
 __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64], float s) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -697,7 +720,8 @@ __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64],
 // grid (nb, BH), 256 threads: per 128-token block, sQ = amax / 448 and
 // Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ...
 __global__ void __launch_bounds__(256) quant_q8_kernel(const uint16_t* q, uint8_t* qhat, float* sq,
-                                                       int N, int Npad, int nb, const int* status) {
+                                                       int N, int Npad, int nb, int hadamard,
+                                                       const int* status) {
   __shared__ float red[8];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x;
@@ -706,6 +730,7 @@ __global__ void __launch_bounds__(256) quant_q8_kernel(const uint16_t* q, uint8_
   if (row < N) load64(q + ((size_t)bh * N + row) * 128 + h * 64, f);
   else
     for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  if (hadamard) hadamard128_pair(f, h);
   float m = 0.0f;
   for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
   const float s = e4m3_scale(block_max(m, red));
@@ -752,7 +777,7 @@ __global__ void key_mean_kernel(const float* ksum, uint16_t* kbar, int N, int nb
 __global__ void __launch_bounds__(256) quant_k8_kernel(const uint16_t* k, const int32_t* perm,
                                                        const uint16_t* kbar, uint8_t* khat,
                                                        float* sk, int N, int Npad, int nb,
-                                                       const int* status) {
+                                                       int hadamard, const int* status) {
   __shared__ float red[8];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x;
@@ -766,6 +791,7 @@ __global__ void __launch_bounds__(256) quant_k8_kernel(const uint16_t* k, const 
   } else {
     for (int i = 0; i < 64; ++i) f[i] = 0.0f;
   }
+  if (hadamard) hadamard128_pair(f, h);
   float m = 0.0f;
   for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
   const float s = e4m3_scale(block_max(m, red));
@@ -953,6 +979,37 @@ __global__ void k4_amax_kernel(const uint16_t* k, const uint16_t* kbar, uint32_t
   if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
 }
 
+// grid (nb, BH), 256 threads: max |x H / sqrt(128)| over the rows of a head
+// (x = Q, or K - kbar when kbar is given; the row order does not matter), as
+// the uint bits of a non-negative float: the 4-bit global scales of the
+// rotated operands.
+__global__ void __launch_bounds__(256) rot_amax_kernel(const uint16_t* x, const uint16_t* kbar,
+                                                       uint32_t* amax_bits, int N,
+                                                       const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
+  float f[64];
+  if (row < N) {
+    load64(x + ((size_t)bh * N + row) * 128 + h * 64, f);
+    if (kbar) {
+      const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  }
+  hadamard128_pair(f, h);
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
+  m = block_max(m, red);
+  if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
+}
+
 // grid BH, 256 threads: the three global scales gq, gk, gr of a head (gr from
 // the per-block residual channel maxima).
 __global__ void g4_kernel(const uint32_t* amax_q, const uint32_t* amax_k, const float* vamax,
@@ -976,7 +1033,7 @@ __global__ void g4_kernel(const uint32_t* amax_q, const uint32_t* amax_k, const 
 // covers row t/2, channels 64*(t%2) ...
 __global__ void __launch_bounds__(256) quant_q4_kernel(const uint16_t* q, const float* g4,
                                                        uint8_t* q4, uint8_t* q4s, int N, int Npad,
-                                                       int nb, const int* status) {
+                                                       int nb, int hadamard, const int* status) {
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x;
   const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
@@ -987,6 +1044,7 @@ __global__ void __launch_bounds__(256) quant_q4_kernel(const uint16_t* q, const 
 #pragma unroll
     for (int i = 0; i < 64; ++i) f[i] = 0.0f;
   }
+  if (hadamard) hadamard128_pair(f, h);
   store64_nvfp4(f, g4[bh * 4 + 0], q4 + ((size_t)bh * Npad + row) * 64 + h * 32,
                 q4s + ((size_t)bh * nb + j) * kScaleTileBytes + scale_tile_off(r, h));
 }
@@ -996,7 +1054,8 @@ __global__ void __launch_bounds__(256) quant_q4_kernel(const uint16_t* q, const 
 __global__ void __launch_bounds__(256) quant_k4_kernel(const uint16_t* k, const int32_t* perm,
                                                        const uint16_t* kbar, const float* g4,
                                                        uint8_t* k4, uint8_t* kr4s, int N,
-                                                       int Npad, int nb, const int* status) {
+                                                       int Npad, int nb, int hadamard,
+                                                       const int* status) {
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x;
   const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
@@ -1011,6 +1070,7 @@ __global__ void __launch_bounds__(256) quant_k4_kernel(const uint16_t* k, const 
 #pragma unroll
     for (int i = 0; i < 64; ++i) f[i] = 0.0f;
   }
+  if (hadamard) hadamard128_pair(f, h);
   store64_nvfp4(f, g4[bh * 4 + 1], k4 + ((size_t)bh * Npad + row) * 64 + h * 32,
                 kr4s + ((size_t)bh * nb + j) * 2 * kScaleTileBytes + scale_tile_off(r, h));
 }
@@ -1190,8 +1250,10 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   float* mut = reinterpret_cast<float*>(S + L.mutilde);
   uint8_t* mside = S + L.mside;
   float* vamax = reinterpret_cast<float*>(S + L.vamax);
-  quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
-  quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, status);
+  const int had = (a.flags & VCA_PREP_QK_HADAMARD) ? 1 : 0;
+  quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, had, status);
+  quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, had,
+                                                status);
   vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
                                               a.reuse != 3 && a.reuse != 4, status);
   vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
@@ -1226,14 +1288,21 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   uint32_t* amax_k = amax_q + BH;
   zero_kernel<<<1, 256, 0, st>>>(amax_q, 2 * (size_t)BH);
   const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
-  head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
-  k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
+  const int had = (a.flags & VCA_PREP_QK_HADAMARD) ? 1 : 0;
+  if (had) {
+    rot_amax_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, nullptr, amax_q, N, status);
+    rot_amax_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, kbar, amax_k, N, status);
+  } else {
+    head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
+    k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
+  }
   vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
                                               a.reuse != 3 && a.reuse != 4, status);
   g4_kernel<<<BH, 256, 0, st>>>(amax_q, amax_k, vamax, g4, nb, status);
-  quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, status);
+  quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, had,
+                                                status);
   quant_k4_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, S + L.k4, S + L.kr4s, N, Npad,
-                                                nb, status);
+                                                nb, had, status);
   const int ngroups = (nb + kGroup4 - 1) / kGroup4;
   zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroup4Bytes / 4, 256, 4096), 256, 0, st>>>(
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroup4Bytes / 4);

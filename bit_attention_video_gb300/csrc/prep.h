@@ -34,6 +34,7 @@ struct PrepArgs {
   const uint16_t* k_in;
   const uint16_t* v;
   int B, H, N, nb, Npad, k, iters, reuse;
+  unsigned flags;  // VCA_PREP_* options
   uint64_t seed;
   uint8_t* state;
   vca_state_layout L;

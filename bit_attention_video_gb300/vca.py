@@ -25,6 +25,8 @@ DEFAULT_ITERS = 10
 DEFAULT_SEED = 0
 # reuse_perm modes of vsmooth_prepare (False / True map to FRESH / REUSE)
 PERM_FRESH, PERM_REUSE, PERM_WARM, PERM_PLAIN, PERM_NAIVE = 0, 1, 2, 3, 4
+# option bits of vsmooth_prepare
+PREP_QK_HADAMARD = 1
 
 
 class VcaError(RuntimeError):
@@ -54,6 +56,9 @@ def lib():
         L.vca_state_layout_get.argtypes = [I] * 6 + [C.POINTER(StateLayout)]
         L.vca_vsmooth_prepare.restype = I
         L.vca_vsmooth_prepare.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, P, S, P]
+        L.vca_vsmooth_prepare_ex.restype = I
+        L.vca_vsmooth_prepare_ex.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, C.c_uint, P,
+                                             S, P]
         for fn in ("vca_attention_fp8", "vca_attention_fp8_exp", "vca_attention_nvfp4"):
             getattr(L, fn).restype = I
             getattr(L, fn).argtypes = [P, S, I, I, I, I, P, P]
@@ -112,11 +117,12 @@ def alloc_state(B, H, N, d, k_clusters, bits, device="cuda") -> torch.Tensor:
 
 
 def vsmooth_prepare(q, k, v, k_clusters, state, reuse_perm=False, bits=8,
-                    iters=DEFAULT_ITERS, seed=DEFAULT_SEED, stream=None):
+                    iters=DEFAULT_ITERS, seed=DEFAULT_SEED, stream=None, flags=0):
+    """flags: 0 or PREP_QK_HADAMARD."""
     B, H, N, d = q.shape
-    _check("vca_vsmooth_prepare", lib().vca_vsmooth_prepare(
+    _check("vca_vsmooth_prepare_ex", lib().vca_vsmooth_prepare_ex(
         _dev(q, torch.bfloat16), _dev(k, torch.bfloat16), _dev(v, torch.bfloat16), B, H, N, d,
-        k_clusters, int(reuse_perm), bits, iters, seed, _dev(state, torch.uint8),
+        k_clusters, int(reuse_perm), bits, iters, seed, flags, _dev(state, torch.uint8),
         state.numel(), _stream(stream)))
 
 
@@ -244,9 +250,10 @@ class VCAttention:
     """Convenience wrapper: owns a state blob for one problem shape."""
 
     def __init__(self, B, H, N, d=128, k_clusters=64, bits=8, iters=DEFAULT_ITERS,
-                 seed=DEFAULT_SEED, device="cuda"):
+                 seed=DEFAULT_SEED, device="cuda", qk_hadamard=False):
         self.shape = (B, H, N, d)
         self.k, self.bits, self.iters, self.seed = k_clusters, bits, iters, seed
+        self.flags = PREP_QK_HADAMARD if qk_hadamard else 0
         self.state = alloc_state(B, H, N, d, k_clusters, bits, device)
 
     def prepare(self, q, k, v, reuse_perm=False, stream=None, iters=None):
@@ -255,7 +262,7 @@ class VCAttention:
         iters overrides the Lloyd iteration count of this call (a warm start
         usually runs fewer)."""
         vsmooth_prepare(q, k, v, self.k, self.state, reuse_perm, self.bits,
-                        self.iters if iters is None else iters, self.seed, stream)
+                        self.iters if iters is None else iters, self.seed, stream, self.flags)
 
     def attention(self, out, stream=None):
         fn = attention_fp8 if self.bits == 8 else attention_nvfp4

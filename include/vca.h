@@ -147,6 +147,26 @@ int vca_vsmooth_prepare(const void* q, const void* k, const void* v, int B, int 
                         int k_clusters, int reuse_perm, int bits, int iters, uint64_t seed,
                         void* state, size_t state_bytes, vca_stream_t stream);
 
+/* Options of vca_vsmooth_prepare_ex. */
+/* The QK Hadamard rotation (paper Appx B: the Q kernel fuses the rotation
+ * before quantisation; the K kernel fuses it after the gather and before the
+ * mean subtraction is quantised): every row of Q and of K' = K[pi] - kbar is
+ * multiplied by H / sqrt(128) (H the 128 x 128 Sylvester-Hadamard matrix)
+ * before its block scale and codes are taken, so QK^T is unchanged in exact
+ * arithmetic.  The rotation is the fast transform in fp32: butterflies
+ * (a, b) -> (a + b, a - b) on channel pairs (i, i + s), i & s = 0, for
+ * s = 1, 2, ..., 64 in that order, then one multiply by fp32(1/sqrt(128)).
+ * The attention calls are unchanged; V is not rotated. */
+#define VCA_PREP_QK_HADAMARD 1u
+
+/* vca_vsmooth_prepare with options: flags is 0 or VCA_PREP_QK_HADAMARD (any
+ * other bit: VCA_ERR_INVALID_ARG).  vca_vsmooth_prepare is this call with
+ * flags = 0; every other argument is the same. */
+int vca_vsmooth_prepare_ex(const void* q, const void* k, const void* v, int B, int H, int N,
+                           int d, int k_clusters, int reuse_perm, int bits, int iters,
+                           uint64_t seed, unsigned flags, void* state, size_t state_bytes,
+                           vca_stream_t stream);
+
 /* 8-bit fused attention (paper §3.1 Eq 1, §3.2 Eq 6, §3.3 Eq 7): FP8 QK'^T
  * and P R on tcgen05 tensor cores, ExpCast-FP8 probability bytes relative to
  * the running row maximum, block means restored from the row sums in the same

@@ -74,6 +74,9 @@ def test_prepare_rejects_bad_arguments(L):
     assert call(kc=300) == -2
     assert call(kc=257 - 1, N=100) == -2
     assert call(sb=nb - 1) == -4
+    a = dict(ok)
+    X = L.vca_vsmooth_prepare_ex
+    assert X(a["q"], a["k"], a["v"], 1, 1, 256, 128, 4, 0, 8, 3, 0, 2, a["state"], nb, None) == -1
 
 
 def test_attention_rejects_bad_arguments(L):

@@ -170,3 +170,45 @@ def test_bf16_reference_matches_exact(orc, B, H, N):
             ref = orc.attention_exact(q[b, h], k[b, h], v[b, h], rows)
             err = rel_l2(bf16_f64(got[b, h][rows]), ref)
             assert err <= 8e-3, f"(b={b},h={h}) relative L2 {err:.3e}"
+
+
+@pytest.mark.parametrize("bits,mode,B,H,N,kc", [
+    (8, "fresh", 1, 2, 1000, 16),
+    (8, "naive", 2, 1, 300, 8),
+    (4, "fresh", 1, 2, 700, 16),
+])
+def test_qk_hadamard_preparation_and_attention(orc, bits, mode, B, H, N, kc):
+    """The QK Hadamard rotation fused into the Q and K quantisers: every
+    operand is bit-exact with the oracle's rotated preparation and the
+    attention matches the oracle on it."""
+    from bit_attention_video_gb300 import vca
+    from test_gpu_prep import check_head8
+    from test_gpu_nvfp4 import check_head4
+    q, k, v = synth.make_qkv(B, H, N, 128, 16, 51)
+    shape = (B, H, N, 128)
+    state = vca.alloc_state(*shape, kc, bits)
+    pm = vca.PERM_NAIVE if mode == "naive" else vca.PERM_FRESH
+    vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), kc, state, pm, bits, 3, 7,
+                        flags=vca.PREP_QK_HADAMARD)
+    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    (vca.attention_fp8 if bits == 8 else vca.attention_nvfp4)(state, shape, out)
+    assert vca.get_status(state) == 0
+    g = {n: t.cpu().numpy() for n, t in vca.state_view(state, shape, kc, bits).items()}
+    got = to_np_u16(out)
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(H):
+            bh = b * H + h
+            prep = orc.prepare8 if bits == 8 else orc.prepare4
+            p = prep(q[b, h], k[b, h], v[b, h], kc, 3, 7, b=b, h=h, H=H, naive=mode == "naive",
+                     hadamard=True)
+            if bits == 8:
+                check_head8(g, p, bh, N, what=("perm",))
+                _, ref = orc.attention8(p, rows)
+                tol = TOL8
+            else:
+                check_head4(g, p, bh, N, what=("perm",))
+                _, ref = orc.attention4(p, rows)
+                tol = 1e-2
+            err = rel_l2(bf16_f64(got[b, h]), ref)
+            assert err <= tol, f"(b={b},h={h}) relative L2 {err:.3e}"
