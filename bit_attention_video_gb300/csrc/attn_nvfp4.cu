@@ -37,9 +37,11 @@
 // Per key block j and tile (log2 domain, a = gq gk log2(e) / sqrt(d)):
 //   M'  = max(M, a rowmax(S))
 //   p'  = 2^(a S - M' + log2 2688)          so that p' <= 2688
-//   r   = sum p'   (fp32, from the unquantised probabilities: Eq 6's r)
+//   r   = sum p'   (from the unquantised probabilities: Eq 6's r; block
+//         sums of 16 in f16, accumulated in fp32)
 //   P   = NVFP4(p'): scale UE4M3(max16 / 6), elements E2M1(p' / scale), each
 //         element evaluated directly as 2^(a S - M' + log2 2688 - log2 scale)
+//         (exponent in fp32, exponential in packed f16)
 //   A  *= alpha = 2^(M - M'), l = alpha l + r
 //   A  += P R_j          (block-scaled FP4 MMA; R = R-codes x scales, no gr)
 //   A  += (r / gr) mu_j  (one BF16 K=16 MMA per group of 4 blocks; the bf16 hi
@@ -47,6 +49,7 @@
 //                         block's mean in K rows 2u, 2u+1)
 // Epilogue: O = gr A / l (l in the same 2688-scaled units), bf16.
 #include "common.cuh"
+#include <cuda_fp16.h>
 #include "prep.h"
 
 namespace vca {
@@ -389,14 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = ex2(M - Mn);   // 0 on the first block
       const float nbias = kLog2P - Mn;
       // Per 16 keys: the block scale from the block maximum, then each code
-      // straight from q = p' / scale = 2^(a s - M' + log2 2688 - log2 scale)
-      // (one FMA and one ex2 per score); the row sum r = sum p' is rebuilt as
-      // scale * sum q per block of 16.  A block whose scale rounds to zero
+      // straight from q = p' / scale = 2^(a s - M' + log2 2688 - log2 scale):
+      // the exponent in fp32, then the exponential, the block sum and the
+      // E2M1 cast on packed f16 pairs (f16 carries q <= 6 to 11 bits, far
+      // finer than E2M1); the row sum r = sum p' is rebuilt as scale * sum q
+      // per block of 16.  A block whose scale rounds to zero
       // holds probabilities below 2688 * 2^-10 / 6 of the maximum: codes 0,
       // and their negligible share of r is dropped.
       float rs = 0.0f;
       uint32_t pw[16];
       uint32_t sc4[2] = {0u, 0u};
+      // the eight block scales first (eight independent chains)
+      float scvs[8], nbis[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float amax = ex2(fmaf(mx16[i], a, nbias));
@@ -404,18 +411,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float scv = e4m3_to_f32((uint8_t)sc);
         float l2s;
         asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2s) : "f"(scv));
-        const float nbi = scv > 0.0f ? nbias - l2s : -INFINITY;
+        scvs[i] = scv;
+        nbis[i] = scv > 0.0f ? nbias - l2s : -INFINITY;
         sc4[i / 4] |= sc << (8 * (i % 4));
-        float rsi = 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float scv = scvs[i], nbi = nbis[i];
+        // pairs of keys: the exponent in fp32 (one paired FMA), then the
+        // exponential, the block sum and the E2M1 cast in packed f16
+        uint32_t hsum = 0u;   // f16x2 partial sums of q
         uint32_t by[8];
+        const uint64_t a2 = ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
+        const uint64_t b2 = ((uint64_t)__float_as_uint(nbi) << 32) | __float_as_uint(nbi);
 #pragma unroll
         for (int c = 0; c < 16; c += 2) {
-          const float q0 = ex2(fmaf(__uint_as_float(s[16 * i + c]), a, nbi));
-          const float q1 = ex2(fmaf(__uint_as_float(s[16 * i + c + 1]), a, nbi));
-          rsi += q0 + q1;
-          by[c / 2] = f32x2_to_e2m1x2(q0, q1);
+          const uint64_t s2 = ((uint64_t)s[16 * i + c + 1] << 32) | s[16 * i + c];
+          uint64_t x2;
+          asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x2) : "l"(s2), "l"(a2), "l"(b2));
+          uint32_t h, e;
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(__uint_as_float((uint32_t)(x2 >> 32))),
+              "f"(__uint_as_float((uint32_t)x2)));
+          asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hsum) : "r"(hsum), "r"(e));
+          uint16_t bb;
+          asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f16x2 t, %1;\ncvt.u16.u8 %0, t;\n}"
+              : "=h"(bb) : "r"(e));
+          by[c / 2] = bb;
         }
-        rs = fmaf(rsi, scv, rs);
+        const float hlo = __half2float(__ushort_as_half((uint16_t)(hsum & 0xFFFFu)));
+        const float hhi = __half2float(__ushort_as_half((uint16_t)(hsum >> 16)));
+        rs = fmaf(hlo + hhi, scv, rs);
         pw[2 * i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
         pw[2 * i + 1] = __byte_perm(__byte_perm(by[4], by[5], 0x0040), __byte_perm(by[6], by[7], 0x0040), 0x5410);
       }
