@@ -288,12 +288,12 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 // K-major (128-byte swizzle) as the A operand of the first product and
 // MN-major as the B operand of the second.
 // Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
-// warp 1 MMA issuer and TMEM owner; warps 4-7 workers, one token row per
-// thread, which convert tile t to fp16 while the tensor core works on tile
-// t-1 and then take tile t-1's argmin and write its one-hot columns.  H^T and
-// D_a are double-buffered and X has nx = 3 buffers when shared memory allows
-// (2 otherwise), so converting a tile waits for the cluster-sum product of
-// the tile nx before it, issued an iteration earlier.  The CTA's cluster sums
+// warp 1 MMA issuer and TMEM owner; warps 8-11 convert each tile to fp16;
+// warps 4-7, one token row per thread (the TMEM lane), take each tile's
+// argmin and write its one-hot columns, so converting tile t+1 overlaps the
+// argmin of tile t.  H^T and D_a are double-buffered and X has nx = 3
+// buffers when shared memory allows (2 otherwise), so converting a tile waits
+// for the cluster-sum product of the tile nx before it.  The CTA's cluster sums
 // D_u and counts are added to the global sums once at the end.
 constexpr int kPipeStages = 3;
 constexpr int kPipeMaxTiles = 1024;                   // 1024 * 128 * 127 < 2^24
@@ -310,7 +310,8 @@ enum { KB_XFULL = 0, KB_XEMPTY = KB_XFULL + kPipeStages, KB_XREADY = KB_XEMPTY +
        KB_DA = KB_XREADY + 3, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
        KB_CNT = KB_UDONE + 3, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int kPipeThreads = 384;
+__global__ void __launch_bounds__(kPipeThreads, 1)
     kmeans_assign_pipe_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t* cent,
                               int32_t* labels, int32_t* sums, int32_t* counts, int N, int k,
                               int kpad, int tiles_per_cta, int nx, int* status) {
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(256, 1)
   // centroids -> fp16, K-major 128-byte swizzle: two atoms of kpad rows x 64
   // channels; rows k..kpad-1 are zero
   const int8_t* cg = cent + (size_t)bh * k * 128;
-  for (int i = tid; i < kpad * 16; i += 256) {  // one 16-byte chunk (8 channels) per step
+  for (int i = tid; i < kpad * 16; i += kPipeThreads) {  // one 16-byte chunk (8 channels) per step
     const int m = i / 16, c8 = i % 16, atom = c8 / 8, ch = c8 % 8;
     uint32_t w[4] = {0, 0, 0, 0};
     if (m < k) {
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(256, 1)
     *reinterpret_cast<uint4*>(sm + kPC + atom * kpad * 128 + m * 128 + ((ch ^ (m & 7)) << 4)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
-  for (int m = tid; m < 128; m += 256) {
+  for (int m = tid; m < 128; m += kPipeThreads) {
     cnt[m] = 0;
     int32_t n2 = 0;
     if (m < k)
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(256, 1)
   }
   // both one-hot buffers start at zero; a worker later clears only the entry
   // it set two tiles before
-  for (int i = tid; i < 2 * 32768 / 16; i += 256)
+  for (int i = tid; i < 2 * 32768 / 16; i += kPipeThreads)
     reinterpret_cast<uint4*>(sm + kPH)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -447,14 +448,12 @@ __global__ void __launch_bounds__(256, 1)
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar(KB_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ workers
-    const int wt = tid - 128, quarter = warp - 4;  // token row / cluster row = TMEM lane
-    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-    int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ converters
+    const int wt = tid - 256;
     bool ok = true;
-    for (int t = 0; t <= nt && ok; ++t) {
-      if (t < nt) {
+    for (int t = 0; t < nt && ok; ++t) {
+      {
         // convert tile t: int8 rows (no swizzle) -> fp16 K-major 128-byte
         // swizzle (channels 0-63 and 64-127 in two 16 KB atoms)
         const int s = t % kPipeStages, xi = t % nx;
@@ -464,27 +463,35 @@ __global__ void __launch_bounds__(256, 1)
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t* src = sm + kPS + s * 16384;
         uint8_t* xb = sm + kPX + xi * 32768;
-#pragma unroll 2
-        for (int u = 0; u < 8; ++u) {
-          const int i = wt + 128 * u, r = i >> 3, c = i & 7;  // row r, 16 channels from 16 c
-          const uint4 in = *reinterpret_cast<const uint4*>(src + r * 128 + c * 16);
-          const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
-          uint32_t w[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) i8x4_to_f16x4(iw[q], w[2 * q], w[2 * q + 1]);
-          uint8_t* dst = xb + (c >> 2) * 16384 + r * 128;
-          const int ch = (c & 3) * 2;
-          *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (r & 7)) << 4)) =
-              make_uint4(w[4], w[5], w[6], w[7]);
+        // one 16-byte chunk (8 channels) per thread and step: a warp covers
+        // two whole rows, so each group of 8 lanes reads 64 contiguous bytes
+        // and writes the 8 (swizzled) chunks of one 128-byte atom row:
+        // no shared-memory bank conflicts
+#pragma unroll 4
+        for (int u = 0; u < 16; ++u) {
+          const int i = wt + 128 * u, r = i >> 4, c8 = i & 15;  // row r, channels 8 c8 ..
+          const uint2 in = *reinterpret_cast<const uint2*>(src + r * 128 + c8 * 8);
+          uint32_t w[4];
+          i8x4_to_f16x4(in.x, w[0], w[1]);
+          i8x4_to_f16x4(in.y, w[2], w[3]);
+          uint8_t* dst = xb + (c8 >> 3) * 16384 + r * 128;
+          *reinterpret_cast<uint4*>(dst + (((c8 & 7) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(KB_XEMPTY + s));
         mbar_arrive(bar(KB_XREADY + xi));
       }
-      if (t >= 1) {
-        // tile t-1: argmin of this token's row of D_a, then its one-hot column
-        const int u = t - 1, b = u & 1;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ argmin workers
+    const int wt = tid - 128, quarter = warp - 4;  // token row / cluster row = TMEM lane
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
+    bool ok = true;
+    for (int u = 0; u < nt && ok; ++u) {
+      {
+        // tile u: argmin of this token's row of D_a, then its one-hot column
+        const int b = u & 1;
         ok = mbar_wait(bar(KB_DA + b), (u >> 1) & 1, &abort_flag, status);
         // H^T[b] was last read by the cluster-sum product of tile u - 2
         if (ok && u >= 2) ok = mbar_wait(bar(KB_UDONE + (u - 2) % nx), ((u - 2) / nx) & 1, &abort_flag, status);
@@ -1190,7 +1197,7 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
       }
       const dim3 grid((T + tpc - 1) / tpc, BH);
       for (int it = 0; it < a.iters; ++it) {
-        kmeans_assign_pipe_kernel<<<grid, 256, psmem, st>>>(tmx, cent, labels, sums, counts, N,
+        kmeans_assign_pipe_kernel<<<grid, kPipeThreads, psmem, st>>>(tmx, cent, labels, sums, counts, N,
                                                              k, kpad, tpc, nx, status);
         kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
       }
