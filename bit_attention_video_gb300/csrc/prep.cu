@@ -708,7 +708,29 @@ __device__ __forceinline__ void hadamard128_pair(float (&f)[64], int h) {
   }
 }
 
+// E4M3 codes (RNE, saturating) of the correctly rounded quotients x / s,
+// mostly without dividing.  With r the rounded reciprocal of s, the products
+// x rlo and x rhi (rlo, rhi = r (1 -/+ 2^-20) rounded) carry at most three
+// roundings of 2^-24 each, so they bracket the rounded quotient in
+// magnitude; the E4M3 cast is monotone in magnitude, so when both ends give
+// the same code it is the quotient's.  Otherwise (a quotient within about
+// 2^-20 of an E4M3 rounding boundary, rare) the division runs exactly.
+struct QuotBracket {
+  float s, rlo, rhi;
+};
+__device__ __forceinline__ QuotBracket quot_bracket(float s) {
+  const float r = __frcp_rn(s);
+  return {s, __fmul_rn(r, 1.0f - 0x1p-20f), __fmul_rn(r, 1.0f + 0x1p-20f)};
+}
+__device__ __forceinline__ uint32_t e4m3x2_quot(float x0, float x1, const QuotBracket& q) {
+  const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x0, q.rlo), __fmul_rn(x1, q.rlo));
+  const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x0, q.rhi), __fmul_rn(x1, q.rhi));
+  if (lo == hi) return lo;
+  return f32x2_to_e4m3x2(__fdiv_rn(x0, q.s), __fdiv_rn(x1, q.s));
+}
+
 __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64], float s) {
+  const QuotBracket qb = quot_bracket(s);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -716,8 +738,8 @@ __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64],
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = q * 16 + e * 4;
-      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s));
-      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(f[i + 2], s), __fdiv_rn(f[i + 3], s));
+      const uint32_t lo = e4m3x2_quot(f[i], f[i + 1], qb);
+      const uint32_t hi = e4m3x2_quot(f[i + 2], f[i + 3], qb);
       w[e] = lo | (hi << 16);
     }
     d[q] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -726,7 +748,7 @@ __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64],
 
 // grid (nb, BH), 256 threads: per 128-token block, sQ = amax / 448 and
 // Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ...
-__global__ void __launch_bounds__(256) quant_q8_kernel(const uint16_t* q, uint8_t* qhat, float* sq,
+__global__ void __launch_bounds__(256, 3) quant_q8_kernel(const uint16_t* q, uint8_t* qhat, float* sq,
                                                        int N, int Npad, int nb, int hadamard,
                                                        const int* status) {
   __shared__ float red[8];
@@ -781,7 +803,7 @@ __global__ void key_mean_kernel(const float* ksum, uint16_t* kbar, int N, int nb
 }
 
 // grid (nb, BH), 256 threads: K' = K[pi] - kbar, per-block E4M3.
-__global__ void __launch_bounds__(256) quant_k8_kernel(const uint16_t* k, const int32_t* perm,
+__global__ void __launch_bounds__(256, 3) quant_k8_kernel(const uint16_t* k, const int32_t* perm,
                                                        const uint16_t* kbar, uint8_t* khat,
                                                        float* sk, int N, int Npad, int nb,
                                                        int hadamard, const int* status) {
@@ -883,6 +905,7 @@ __global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const in
   const size_t o = ((size_t)bh * nb + j) * 128 + c;
   const float mf = bf16_bits_to_f32(mu[o]);
   const float s = sv[(size_t)bh * 128 + c];
+  const QuotBracket qb = quot_bracket(s);
   uint4* dst = reinterpret_cast<uint4*>(rhatT + ((size_t)bh * 128 + c) * Npad + (size_t)j * 128);
 #pragma unroll 2
   for (int q = 0; q < 8; ++q) {
@@ -893,9 +916,9 @@ __global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const in
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int r = q * 16 + e * 4 + u;
-        y[u] = (j * 128 + r < N) ? __fdiv_rn(__fsub_rn(bf16_bits_to_f32(tile[r][c]), mf), s) : 0.0f;
+        y[u] = (j * 128 + r < N) ? __fsub_rn(bf16_bits_to_f32(tile[r][c]), mf) : 0.0f;
       }
-      w[e] = (uint32_t)f32x2_to_e4m3x2(y[0], y[1]) | ((uint32_t)f32x2_to_e4m3x2(y[2], y[3]) << 16);
+      w[e] = e4m3x2_quot(y[0], y[1], qb) | (e4m3x2_quot(y[2], y[3], qb) << 16);
     }
     dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
