@@ -952,11 +952,19 @@ __device__ __forceinline__ uint32_t nvfp4_16(const float* x, float g, uint2& pac
   const float scv = e4m3_to_f32((uint8_t)sc);
   uint32_t w[2] = {0u, 0u};
   if (scv > 0.0f) {
+    // E2M1 codes of the rounded quotients x / step through the same
+    // bracketing products as the E4M3 quantisers (the E2M1 cast is monotone
+    // in magnitude too)
     const float step = __fmul_rn(scv, g);
+    const float r = __frcp_rn(step);
+    const float rlo = __fmul_rn(r, 1.0f - 0x1p-20f), rhi = __fmul_rn(r, 1.0f + 0x1p-20f);
 #pragma unroll
-    for (int i = 0; i < 16; i += 2)
-      w[i / 8] |= (uint32_t)f32x2_to_e2m1x2(__fdiv_rn(x[i], step), __fdiv_rn(x[i + 1], step))
-                  << (4 * (i % 8));
+    for (int i = 0; i < 16; i += 2) {
+      uint32_t c = f32x2_to_e2m1x2(__fmul_rn(x[i], rlo), __fmul_rn(x[i + 1], rlo));
+      if (c != f32x2_to_e2m1x2(__fmul_rn(x[i], rhi), __fmul_rn(x[i + 1], rhi)))
+        c = f32x2_to_e2m1x2(__fdiv_rn(x[i], step), __fdiv_rn(x[i + 1], step));
+      w[i / 8] |= c << (4 * (i % 8));
+    }
   }
   packed = make_uint2(w[0], w[1]);
   return sc;

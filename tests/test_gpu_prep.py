@@ -166,3 +166,25 @@ def test_reuse_without_cached_permutation_is_reported(orc):
     big[:state2.numel()].copy_(state2)
     vca.vsmooth_prepare(to_dev(q), to_dev(k), to_dev(v), 4, big, True, 8, 2, 0)
     assert vca.get_status(big) == -5
+
+
+def test_quantiser_rounding_boundaries(orc):
+    """Quotients on E4M3 rounding midpoints: every 128-row block of Q holds
+    448 (so its scale is exactly 1) and values halfway between two E4M3 codes,
+    which the quantiser must round to even exactly as the oracle's division
+    does (the reciprocal shortcut cannot decide them)."""
+    B, H, N, kc = 1, 1, 512, 4
+    q, k, v = synth.make_qkv(B, H, N, 128, 4, 77)
+    rng = np.random.default_rng(5)
+    mids = np.array([1 + (2 * m + 1) / 16 for m in range(8)] +
+                    [2 * (1 + (2 * m + 1) / 16) for m in range(8)], np.float32)
+    vals = rng.choice(np.concatenate([mids, -mids]), size=(N, 128)).astype(np.float32)
+    vals[::128, 0] = 448.0
+    q = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q = np.ascontiguousarray(q.reshape(B, H, N, 128))
+    _, st, g = gpu_prepare(q, k, v, kc, 2, 3)
+    assert st == 0
+    p = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], kc, 2, 3)
+    assert np.all(p["sq"] == 1.0)
+    assert np.array_equal(g["qhat"][0], p["qhat"])
+    assert np.array_equal(g["sq"][0], p["sq"])
