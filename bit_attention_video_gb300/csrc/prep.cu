@@ -133,6 +133,12 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
   const uint4* src = reinterpret_cast<const uint4*>(v + bh * per_head);
   uint2* dst = reinterpret_cast<uint2*>(x + bh * per_head);
   const size_t n8 = per_head / 8;
+  // RNE(v / s) from the bracketing products v rlo <= RN(v / s) <= v rhi (in
+  // magnitude; rlo, rhi = (1/s)(1 -/+ 2^-20) rounded): integer rounding is
+  // monotone, so equal integers at both ends are the quotient's; each end is
+  // rounded to the integer grid by adding 1.5 * 2^23 (|v / s| <= 127).
+  const float r = __frcp_rn(s);
+  const float rlo = __fmul_rn(r, 1.0f - 0x1p-20f), rhi = __fmul_rn(r, 1.0f + 0x1p-20f);
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
        i += (size_t)gridDim.x * blockDim.x) {
     uint4 w = src[i];
@@ -141,7 +147,10 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const uint32_t bits = (e & 1) ? (ws[e / 2] & 0xFFFF0000u) : (ws[e / 2] << 16);
-      int q = __float2int_rn(__fdiv_rn(__uint_as_float(bits), s));
+      const float xv = __uint_as_float(bits);
+      const float a = __fadd_rn(__fmul_rn(xv, rlo), 12582912.0f);
+      const float b = __fadd_rn(__fmul_rn(xv, rhi), 12582912.0f);
+      int q = a == b ? (int)(__float_as_uint(a) - 0x4B400000u) : __float2int_rn(__fdiv_rn(xv, s));
       q = max(-127, min(127, q));
       out[e / 4] |= ((uint32_t)(q & 0xFF)) << (8 * (e % 4));
     }
