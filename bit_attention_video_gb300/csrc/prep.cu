@@ -497,6 +497,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
     int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
     bool ok = true;
+    float cn[64];   // ||c_m||^2 (+inf past k), used when kpad <= 64
+#pragma unroll
+    for (int m = 0; m < 64; ++m) cn[m] = m < k ? cnorm[m & 127] : INFINITY;
     for (int u = 0; u < nt && ok; ++u) {
       {
         // tile u: argmin of this token's row of D_a, then its one-hot column
@@ -511,16 +514,36 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         // the strict comparison keeps the lowest index on ties
         float best = INFINITY;
         int bestm = 0;
-        for (int c0 = 0; c0 < kpad; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(trow + c0, v);
+        if (kpad <= 64) {
+          // the squared norms in registers (loaded once), both halves of D_a
+          // in flight, four independent running minima over interleaved
+          // clusters merged in index order at the end
+          uint32_t v[64];
+          tmem_ld32(trow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          if (kpad > 32) tmem_ld32(trow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_ld_wait();
+          float bq[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+          int mq[4] = {0, 1, 2, 3};
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int m = c0 + c;
-            if (m < k) {
-              const float dist = fmaf(-2.0f, __uint_as_float(v[c]), cnorm[m]);
-              if (dist < best) { best = dist; bestm = m; }
+          for (int m = 0; m < 64; ++m) {
+            const float dist = fmaf(-2.0f, __uint_as_float(v[m]), cn[m]);
+            if (m < kpad && dist < bq[m % 4]) { bq[m % 4] = dist; mq[m % 4] = m; }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (bq[q] < best || (bq[q] == best && mq[q] < bestm)) { best = bq[q]; bestm = mq[q]; }
+        } else {
+          for (int c0 = 0; c0 < kpad; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(trow + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int m = c0 + c;
+              if (m < k) {
+                const float dist = fmaf(-2.0f, __uint_as_float(v[c]), cnorm[m]);
+                if (dist < best) { best = dist; bestm = m; }
+              }
             }
           }
         }

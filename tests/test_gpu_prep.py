@@ -65,6 +65,7 @@ def check_head8(g, p, bh, N, what=("labels", "perm", "centroids")):
     (1, 1, 128, 4, 4, 2),        # exactly one block
     (1, 3, 1, 1, 1, 1),          # one token
     (1, 1, 2500, 64, 200, 2),    # k > 96 (single accumulator group), several sort chunks
+    (1, 2, 1300, 64, 96, 3),     # 64 < k <= 128: the tensor-core Lloyd step, two D_a chunks
 ])
 def test_prepare8_bit_exact(orc, B, H, N, C, kc, iters):
     seed = 0xC0FFEE + N
