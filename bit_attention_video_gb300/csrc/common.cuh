@@ -318,9 +318,10 @@ __host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (b_mn_major ? (1u << 16) : 0u) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false,
+                                                 bool a_mn_major = false) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (a_mn_major ? (1u << 15) : 0u) |
+         (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major = false) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |

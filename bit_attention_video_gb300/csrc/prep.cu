@@ -292,10 +292,10 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 // per-CTA sum of at most kPipeMaxTiles tiles stays below 2^24), per tile:
 //   D_a = X C^T       (M = 128 tokens, N = kpad centroids, K = 128 channels)
 //   label_t = argmin_m ||c_m||^2 - 2 D_a[t, m]  (lowest index on ties)
-//   D_u += H^T X      (M = 128 cluster rows, N = 128 channels, K = 128 tokens)
+//   D_u += X^T H      (M = 128 channels, N = kpad clusters, K = 128 tokens)
 // with H the one-hot label matrix.  The X tile is one shared-memory image:
 // K-major (128-byte swizzle) as the A operand of the first product and
-// MN-major as the B operand of the second.
+// MN-major as the A operand of the second; H is stored K-major as H^T.
 // Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
 // warp 1 MMA issuer and TMEM owner; warps 8-11 convert each tile to fp16;
 // warps 4-7, one token row per thread (the TMEM lane), take each tile's
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // per step t: assign(t) once tile t is converted, update(t-1) once its
     // one-hot columns are written
-    const uint32_t ia = idesc_f16(128, kpad), iu = idesc_f16(128, 128, true);
+    const uint32_t ia = idesc_f16(128, kpad), iu = idesc_f16(128, kpad, false, true);
     bool ok = true;
     for (int t = 0; t <= nt && ok; ++t) {
       if (t < nt) {
@@ -447,8 +447,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         const uint32_t xb = base + kPX + (u % nx) * 32768, hb = base + kPH + b * 32768;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_f16_ss_w(tmem + col_u, desc_k_sw128(hb + (s / 4) * 16384 + (s % 4) * 32),
-                       make_desc(xb + s * 2048, 16384, 1024, 2), iu, (u > 0 || s > 0));
+          mma_f16_ss_w(tmem + col_u, make_desc(xb + s * 2048, 16384, 1024, 2),
+                       desc_k_sw128(hb + (s / 4) * 16384 + (s % 4) * 32), iu, (u > 0 || s > 0));
         mma_commit_w(bar(KB_UDONE + u % nx));
       }
     }
@@ -567,25 +567,26 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         mbar_arrive(bar(KB_HREADY + b));
       }
     }
-    // the CTA's cluster sums (TMEM lane m = cluster m) and counts
+    // the CTA's cluster sums (TMEM lane c = channel c, column m = cluster m)
+    // and counts
     mbar_arrive(bar(KB_CNT));
     if (ok) ok = mbar_wait(bar(KB_UDONE + (nt - 1) % nx), ((nt - 1) / nx) & 1, &abort_flag, status);
     if (ok) ok = mbar_wait(bar(KB_CNT), 0, &abort_flag, status);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      const int m = wt;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      const int c = wt;
+      for (int m0 = 0; m0 < kpad; m0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lanes + col_u + c0, v);
+        tmem_ld32(tmem + lanes + col_u + m0, v);
         tmem_ld_wait();
-        if (m < k && cnt[m] > 0)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int sv = (int)__uint_as_float(v[c]);
-            if (sv) atomicAdd(&sums[((size_t)bh * k + m) * 128 + c0 + c], sv);
-          }
+        for (int i = 0; i < 32; ++i) {
+          const int m = m0 + i;
+          const int sv = (int)__uint_as_float(v[i]);
+          if (m < k && sv) atomicAdd(&sums[((size_t)bh * k + m) * 128 + c], sv);
+        }
       }
-      if (m < k && cnt[m]) atomicAdd(&counts[(size_t)bh * k + m], cnt[m]);
+      if (wt < k && cnt[wt]) atomicAdd(&counts[(size_t)bh * k + wt], cnt[wt]);
     }
   }
   tc_fence_before();
