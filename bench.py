@@ -46,8 +46,8 @@ ATTN_TRAFFIC = {
     8: dict(bytes=154.314496e6 + 67.907584e6, tokens=24 * 16384,
             sources={"attn_fp8.cu": "a181635ea030b3dd1f424ac9bb7abc6b327b3a062847e1ca4d24c4f722499b3f",
                      "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"}),
-    4: dict(bytes=88.280320e6 + 52.350976e6, tokens=24 * 16384,
-            sources={"attn_nvfp4.cu": "d6a319a3ebc46b74895063894dba3d4f453e5cbd32d3ceeea567c3fc340ac539"}),
+    4: dict(bytes=88.149760e6 + 51.991040e6, tokens=24 * 16384,
+            sources={"attn_nvfp4.cu": "ad04e13f0a71a2630eb0b63400a2385b0e8906104c3ab5a438cace9cdb53c9ff"}),
 }
 
 
