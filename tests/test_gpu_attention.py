@@ -212,3 +212,46 @@ def test_qk_hadamard_preparation_and_attention(orc, bits, mode, B, H, N, kc):
                 tol = 1e-2
             err = rel_l2(bf16_f64(got[b, h]), ref)
             assert err <= tol, f"(b={b},h={h}) relative L2 {err:.3e}"
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_degenerate_values(orc, bits):
+    """Degenerate inputs with known outputs at both bit widths: a value
+    tensor constant per channel is all block mean (the residual and its
+    codes are zero), so every output row is that constant; all-zero values
+    give zero outputs; all-zero queries give uniform attention, the mean
+    of V.  Each also matches the oracle."""
+    from bit_attention_video_gb300 import vca
+    B, H, N, kc = 1, 2, 700, 8
+    q, k, v = synth.make_qkv(B, H, N, 128, 8, 61)
+    rng = np.random.default_rng(9)
+    const = rng.standard_normal((H, 128)).astype(np.float32)
+    cases = {
+        "constant_v": (q, k, np.broadcast_to(
+            torch.from_numpy(const).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            [None, :, None, :], v.shape).copy()),
+        "zero_v": (q, k, np.zeros_like(v)),
+        "zero_q": (np.zeros_like(q), k, v),
+    }
+    tol = 2e-3 if bits == 8 else 1e-2
+    for name, (qq, kk, vv) in cases.items():
+        att = vca.VCAttention(B, H, N, 128, k_clusters=kc, bits=bits, iters=3)
+        out = att(to_dev(qq), to_dev(kk), to_dev(vv))
+        assert att.status() == 0, name
+        got = bf16_f64(to_np_u16(out))
+        for h in range(H):
+            prep = orc.prepare8 if bits == 8 else orc.prepare4
+            attn = orc.attention8 if bits == 8 else orc.attention4
+            p = prep(qq[0, h], kk[0, h], vv[0, h], kc, 3, 0, b=0, h=h, H=H)
+            _, ref = attn(p, np.arange(N))
+            if name == "zero_v":
+                assert np.all(got[0, h] == 0), name
+                assert np.all(ref == 0), name
+                continue
+            if name == "constant_v":
+                want = np.broadcast_to(bf16_f64(vv[0, h, 0]), (N, 128))
+                assert np.max(np.abs(got[0, h] - want)) <= 2.0 ** -7 * np.max(np.abs(want)), name
+            if name == "zero_q":
+                want = np.broadcast_to(bf16_f64(vv[0, h]).mean(0), (N, 128))
+                assert rel_l2(got[0, h], want) <= (0.02 if bits == 8 else 0.1), name
+            assert rel_l2(got[0, h], ref) <= tol, name
