@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         // two whole rows, so each group of 8 lanes reads 64 contiguous bytes
         // and writes the 8 (swizzled) chunks of one 128-byte atom row:
         // no shared-memory bank conflicts
-#pragma unroll 4
+#pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int i = wt + 128 * u, r = i >> 4, c8 = i & 15;  // row r, channels 8 c8 ..
           const uint2 in = *reinterpret_cast<const uint2*>(src + r * 128 + c8 * 8);
@@ -497,9 +497,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
     int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
     bool ok = true;
-    float cn[64];   // ||c_m||^2 (+inf past k), used when kpad <= 64
+    // used when kpad <= 64: ||c_m||^2 + 2^23 + 2^21 for a cluster, 1.5 * 2^24 past k
+    float cn[64];
 #pragma unroll
-    for (int m = 0; m < 64; ++m) cn[m] = m < k ? cnorm[m & 127] : INFINITY;
+    for (int m = 0; m < 64; ++m) cn[m] = m < k ? cnorm[m & 127] + 10485760.0f : 25165824.0f;
     for (int u = 0; u < nt && ok; ++u) {
       {
         // tile u: argmin of this token's row of D_a, then its one-hot column
@@ -515,23 +516,37 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         float best = INFINITY;
         int bestm = 0;
         if (kpad <= 64) {
-          // the squared norms in registers (loaded once), both halves of D_a
-          // in flight, four independent running minima over interleaved
-          // clusters merged in index order at the end
+          // one packed key per cluster, minimised over a tree.  With x and c
+          // in [-127, 127]^128, d = ||c||^2 - 2 x.c lies in [-||x||^2,
+          // 6193536] and ||x||^2 <= 2064512, so f = d + 2^23 + 2^21 is an
+          // integer in [2^23, 2^24): exact in fp32, its low 23 bits are
+          // f - 2^23, and (bits(f) << 6) + m orders by (d, m), lowest index
+          // on ties.  A zero centroid row past k gives f = 1.5 * 2^24 (key
+          // >= 0xE0000000, above every cluster's); columns past kpad hold
+          // other data and are forced to the largest key.
           uint32_t v[64];
           tmem_ld32(trow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          if (kpad > 32) tmem_ld32(trow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_ld_wait();
-          float bq[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
-          int mq[4] = {0, 1, 2, 3};
+          if (kpad > 32) {
+            tmem_ld32(trow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          } else {
 #pragma unroll
-          for (int m = 0; m < 64; ++m) {
-            const float dist = fmaf(-2.0f, __uint_as_float(v[m]), cn[m]);
-            if (m < kpad && dist < bq[m % 4]) { bq[m % 4] = dist; mq[m % 4] = m; }
+            for (int m = 32; m < 64; ++m) v[m] = 0u;
+          }
+          tmem_ld_wait();
+          uint32_t key[64];
+#pragma unroll
+          for (int m = 0; m < 64; ++m)
+            key[m] = (__float_as_uint(fmaf(-2.0f, __uint_as_float(v[m]), cn[m])) << 6) + (uint32_t)m;
+          if (kpad < 64) {
+#pragma unroll
+            for (int m = 16; m < 64; ++m)
+              if (m >= kpad) key[m] = 0xFFFFFFFFu;
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (bq[q] < best || (bq[q] == best && mq[q] < bestm)) { best = bq[q]; bestm = mq[q]; }
+          for (int s = 32; s >= 1; s >>= 1)
+#pragma unroll
+            for (int m = 0; m < s; ++m) key[m] = min(key[m], key[m + s]);
+          bestm = (int)(key[0] & 63u);
         } else {
           for (int c0 = 0; c0 < kpad; c0 += 32) {
             uint32_t v[32];

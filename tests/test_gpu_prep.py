@@ -66,6 +66,7 @@ def check_head8(g, p, bh, N, what=("labels", "perm", "centroids")):
     (1, 3, 1, 1, 1, 1),          # one token
     (1, 1, 2500, 64, 200, 2),    # k > 96 (single accumulator group), several sort chunks
     (1, 2, 1300, 64, 96, 3),     # 64 < k <= 128: the tensor-core Lloyd step, two D_a chunks
+    (1, 1, 700, 24, 24, 3),      # 16 < k <= 32: one 32-column D_a load
 ])
 def test_prepare8_bit_exact(orc, B, H, N, C, kc, iters):
     seed = 0xC0FFEE + N
@@ -76,6 +77,31 @@ def test_prepare8_bit_exact(orc, B, H, N, C, kc, iters):
         for h in range(H):
             p = orc.prepare8(q[b, h], k[b, h], v[b, h], kc, iters, seed, b=b, h=h, H=H)
             check_head8(g, p, b * H + h, N)
+
+
+@pytest.mark.parametrize("kc", [3, 33])
+def test_kmeans_extreme_distances(orc, kc):
+    """Value tokens on the vertices of the feature cube (every channel
+    +-amax, so every feature is +-127), half of them at the two all-equal
+    corners: the squared-distance offsets
+    ||c||^2 - 2 x.c reach both ends of their range, -128 * 127^2 and
+    3 * 128 * 127^2, and the labels, permutation and operands must still be
+    bit-exact with the oracle's."""
+    B, H, N = 1, 2, 900
+    q, k, v = synth.make_qkv(B, H, N, 128, 8, 31)
+    rng = np.random.default_rng(31)
+    amax = 2.5
+    signs = rng.choice([-1.0, 1.0], size=(B, H, N, 1))
+    mixed = np.where(rng.random((B, H, N, 128)) < 0.8, signs, -signs)
+    corner = np.where(rng.random((B, H, N, 1)) < 0.5, signs, mixed)  # half of them pure corners
+    vals = (amax * corner).astype(np.float32)
+    v = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    v = np.ascontiguousarray(v)
+    _, st, g = gpu_prepare(q, k, v, kc, 4, 17)
+    assert st == 0
+    for h in range(H):
+        p = orc.prepare8(q[0, h], k[0, h], v[0, h], kc, 4, 17, b=0, h=h, H=H)
+        check_head8(g, p, h, N)
 
 
 def test_prepare8_h8_sampled_heads(orc):
