@@ -74,6 +74,12 @@ def attn_traffic(w):
     return ref["bytes"] * (w.B * w.H * w.N) / ref["tokens"]
 
 
+# device staging slots of the end-to-end pipeline: a host copy that stalls
+# (page-locked memory that sat idle) is absorbed by the compute of the steps
+# in between
+E2E_SLOTS = 4
+
+
 def grouping_mode(args) -> str:
     if args.naive:
         return "naive"
@@ -338,63 +344,44 @@ def run_gpu(args, w):
     tc_peak = pk["bf16_sus"] * PER_BF16[w.bits]
     pname = PEAK_NAME[w.bits]
 
-    # End to end through the public API, as a serving loop runs it: every step
-    # copies its Q, K, V from pinned host memory, prepares, runs the attention
-    # and reads its O back to pinned host memory.  Two device buffer sets and
-    # a copy stream let step i+1's input copies and step i's result copy
-    # overlap the compute of the neighbouring step.
+    # End to end through the C ABI's host-buffer pipeline (vca_pipeline_*), as a
+    # serving loop runs it: every step copies its Q, K, V from pinned host
+    # memory into one of E2E_SLOTS device staging slots, prepares, runs the
+    # attention and reads its O back into pinned host memory; the copies of
+    # later steps and the read-backs of earlier ones overlap the compute.
+    # Timed on the host clock from the first submit to the flush that returns
+    # once the last O is in host memory.
     def time_e2e_pipelined():
-        # two created streams: the legacy default stream would serialise with both
-        # (and one stream per copy direction, so step i+1's inputs do not queue
-        # behind step i's output copy)
-        cstream = torch.cuda.Stream(device=dev)
-        copy_stream = torch.cuda.Stream(device=dev)
-        d2h_stream = torch.cuda.Stream(device=dev)
-        cstream.wait_stream(stream)
-        bufs = [[torch.empty_like(x) for x in (q, k, v, out)] for _ in range(2)]
-        outs_host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        consumed = [torch.cuda.Event() for _ in range(2)]
-        d2h_done = [torch.cuda.Event() for _ in range(2)]
+        pipe = vca.HostPipeline(*shape, k_clusters=w.k, bits=w.bits, slots=E2E_SLOTS,
+                                iters=args.iters, seed=0, qk_hadamard=args.qk_hadamard,
+                                fp8_exp=exp_bytes(args), device=dev)
+        outs_host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+                     for _ in range(E2E_SLOTS)]
+        first = [True]
 
         def run(n):
             for i in range(n):
-                b = bufs[i % 2]
-                with torch.cuda.stream(copy_stream):
-                    if i >= 2:
-                        copy_stream.wait_event(consumed[i % 2])   # step i-2 read its inputs
-                    for h, d in zip(host, b[:3]):
-                        d.copy_(h, non_blocking=True)
-                    in_ready[i % 2].record(copy_stream)
-                cstream.wait_event(in_ready[i % 2])
-                if i >= 2:
-                    cstream.wait_event(d2h_done[i % 2])           # step i-2's O was read back
-                att.prepare(b[0], b[1], b[2], stream=cstream, **prep_args())
-                attn_fn(att.state, shape, b[3], stream=cstream)
-                consumed[i % 2].record(cstream)
-                with torch.cuda.stream(d2h_stream):
-                    d2h_stream.wait_event(consumed[i % 2])
-                    outs_host[i % 2].copy_(b[3], non_blocking=True)
-                    d2h_done[i % 2].record(d2h_stream)
-            cstream.wait_stream(copy_stream)
-            cstream.wait_stream(d2h_stream)
+                if first[0] and mode != vca.PERM_NAIVE:
+                    kw = dict(reuse_perm=vca.PERM_FRESH)
+                else:
+                    kw = dict(reuse_perm=mode, iters=grouping_iters(args))
+                first[0] = False
+                pipe.submit(host[0], host[1], host[2], outs_host[i % E2E_SLOTS], **kw)
+            pipe.flush()
 
-        run(2)
-        torch.cuda.synchronize()
+        run(E2E_SLOTS)
         if dist:
             dist.barrier()
-        # three timed runs of `steps` steps each; the median is reported (the
-        # host's copy engines are shared with other jobs, and a single run
-        # can catch a stall of one copy)
+        # three timed runs; the median is reported (the host's copy engines and
+        # memory are shared with other jobs)
         runs = []
         for _ in range(3):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(cstream)
-            run(args.steps)
-            e1.record(cstream)
             torch.cuda.synchronize()
-            runs.append(max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev))
+            t0 = time.perf_counter()
+            run(args.e2e_steps)
+            t1 = time.perf_counter()
+            runs.append(max_over_ranks((t1 - t0) * 1e3 / args.e2e_steps, dist, dev))
+        pipe.close()
         return statistics.median(runs), runs
 
     e2e_ms, e2e_runs = None, None
@@ -454,8 +441,12 @@ def run_gpu(args, w):
                  "ms_per_step": e2e_ms, "runs_ms_per_step": e2e_runs,
                  "h2d_bytes_per_step": 3 * nbytes,
                  "d2h_bytes_per_step": nbytes,
-                 "overlap": "pinned copies on a second stream: step i+1's inputs and step i's "
-                            "output move during the neighbouring step's compute"}
+                 "steps_per_run": args.e2e_steps,
+                 "api": "vca_pipeline_submit / vca_pipeline_flush (host buffers)",
+                 "overlap": f"{E2E_SLOTS} device staging slots, one copy stream per direction: "
+                            "later steps' inputs and earlier steps' outputs move during the "
+                            "compute; host clock from the first submit to the last O in host "
+                            "memory"}
                 if e2e_ms else None),
         "gpu_launches": launches_per_step(grouping_iters(args), not groups(args), w.bits)
         * args.steps,
@@ -495,6 +486,8 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=30,
+                    help="steps per timed end-to-end run (the pipeline fills and drains once per run)")
     args = ap.parse_args()
     if args.reuse + args.warm + args.plain + args.naive > 1:
         ap.error("--reuse, --warm, --plain and --naive exclude each other")

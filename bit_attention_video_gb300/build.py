@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvca.so")
-SOURCES = ["api.cu", "prep.cu", "attn_fp8.cu", "attn_bf16.cu", "attn_nvfp4.cu", "debug.cu"]
+SOURCES = ["api.cu", "prep.cu", "attn_fp8.cu", "attn_bf16.cu", "attn_nvfp4.cu", "debug.cu",
+           "pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-diag-suppress", "177"]

@@ -27,6 +27,8 @@ DEFAULT_SEED = 0
 PERM_FRESH, PERM_REUSE, PERM_WARM, PERM_PLAIN, PERM_NAIVE = 0, 1, 2, 3, 4
 # option bits of vsmooth_prepare
 PREP_QK_HADAMARD = 1
+# option bit of HostPipeline (vca_pipeline_submit): the conventional exp-then-cast FP8 product
+PIPELINE_FP8_EXP = 0x100
 
 
 class VcaError(RuntimeError):
@@ -76,6 +78,21 @@ def lib():
         L.vca_debug_mma.argtypes = [I, P, P, P, P]
         L.vca_kmeans_permutation_noalloc.restype = I
         L.vca_kmeans_permutation_noalloc.argtypes = [P, I, I, I, I, U64, I, I, I, P, P, P]
+        L.vca_pipeline_workspace_bytes.restype = S
+        L.vca_pipeline_workspace_bytes.argtypes = [I] * 7
+        L.vca_pipeline_create.restype = I
+        L.vca_pipeline_create.argtypes = [I] * 7 + [P, S, P, C.POINTER(C.c_void_p)]
+        L.vca_pipeline_submit.restype = I
+        L.vca_pipeline_submit.argtypes = [P, P, P, P, P, I, I, U64, C.c_uint,
+                                          C.POINTER(C.c_int64)]
+        L.vca_pipeline_wait.restype = I
+        L.vca_pipeline_wait.argtypes = [P, C.c_int64]
+        L.vca_pipeline_flush.restype = I
+        L.vca_pipeline_flush.argtypes = [P]
+        L.vca_pipeline_state.restype = P
+        L.vca_pipeline_state.argtypes = [P]
+        L.vca_pipeline_destroy.restype = I
+        L.vca_pipeline_destroy.argtypes = [P]
         _lib = L
     return _lib
 
@@ -244,6 +261,74 @@ def state_view(state: torch.Tensor, shape, k_clusters, bits=8) -> dict:
             g4=v(L.g4, BH * 4, torch.float32, (BH, 4)),
         )
     return out
+
+
+def pipeline_workspace_bytes(B, H, N, d, k_clusters, bits, slots) -> int:
+    return lib().vca_pipeline_workspace_bytes(B, H, N, d, k_clusters, bits, slots)
+
+
+def _host(t: torch.Tensor):
+    assert t.device.type == "cpu" and t.is_contiguous() and t.dtype == torch.bfloat16, \
+        "expected a contiguous bf16 host tensor"
+    return C.c_void_p(t.data_ptr())
+
+
+class HostPipeline:
+    """The serving loop's end-to-end call (vca_pipeline_*): each submit takes
+    Q, K, V from host tensors (page-locked for overlap), runs the V-Smooth
+    preparation and the attention of `bits`, and writes O to a host tensor;
+    steps rotate over `slots` device staging slots so that copies overlap the
+    compute of neighbouring steps.  O of step s is valid after wait(s) or
+    flush()."""
+
+    def __init__(self, B, H, N, d=128, k_clusters=64, bits=8, slots=4, iters=DEFAULT_ITERS,
+                 seed=0, qk_hadamard=False, fp8_exp=False, stream=None, device="cuda"):
+        self.shape = (B, H, N, d)
+        self.bits, self.iters, self.seed = bits, iters, seed
+        self.flags = (PREP_QK_HADAMARD if qk_hadamard else 0) | (PIPELINE_FP8_EXP if fp8_exp else 0)
+        nb = pipeline_workspace_bytes(B, H, N, d, k_clusters, bits, slots)
+        if nb == 0:
+            raise VcaError("vca_pipeline_workspace_bytes", -1)
+        self.workspace = torch.empty(nb, dtype=torch.uint8, device=device)
+        self._stream = stream if stream is not None else torch.cuda.current_stream(device)
+        self._p = C.c_void_p()
+        _check("vca_pipeline_create", lib().vca_pipeline_create(
+            B, H, N, d, k_clusters, bits, slots, C.c_void_p(self.workspace.data_ptr()), nb,
+            C.c_void_p(self._stream.cuda_stream), C.byref(self._p)))
+        self._held = {}   # step -> host tensors, kept alive until the step is waited for
+        self.state = self.workspace[:state_bytes(B, H, N, d, k_clusters, bits)]
+
+    def submit(self, q, k, v, out, reuse_perm=False, iters=None) -> int:
+        for t in (q, k, v, out):
+            assert tuple(t.shape) == self.shape, f"expected shape {self.shape}"
+        step = C.c_int64()
+        _check("vca_pipeline_submit", lib().vca_pipeline_submit(
+            self._p, _host(q), _host(k), _host(v), _host(out), int(reuse_perm),
+            self.iters if iters is None else iters, self.seed, self.flags, C.byref(step)))
+        self._held[step.value] = (q, k, v, out)
+        return step.value
+
+    def wait(self, step):
+        _check("vca_pipeline_wait", lib().vca_pipeline_wait(self._p, step))
+        for s in [s for s in self._held if s <= step]:
+            del self._held[s]
+
+    def flush(self):
+        _check("vca_pipeline_flush", lib().vca_pipeline_flush(self._p))
+        self._held.clear()
+
+    def close(self):
+        if self._p:
+            rc = lib().vca_pipeline_destroy(self._p)
+            self._p = C.c_void_p()
+            self._held.clear()
+            _check("vca_pipeline_destroy", rc)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class VCAttention:

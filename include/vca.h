@@ -15,8 +15,10 @@
  * Conventions for every function below
  *   - Tensors Q, K, V, O are bf16, shape [B, H, N, d], contiguous row-major,
  *     d fastest.  Device pointers must be 16-byte aligned.
- *   - All memory is caller-owned.  The library never allocates, frees or
- *     synchronises, except vca_get_status, which synchronises `stream`.
+ *   - All device memory is caller-owned.  The library never allocates, frees
+ *     or synchronises, except vca_get_status, which synchronises `stream`, and
+ *     the host-buffer pipeline (vca_pipeline_*), which owns its streams and
+ *     events and blocks in vca_pipeline_wait / _flush.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Argument errors are returned synchronously, before any
  *     launch; a launch failure returns VCA_ERR_CUDA.  Data-dependent failures
@@ -230,6 +232,84 @@ const char* vca_status_string(int status);
 int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters, int iters,
                                    uint64_t seed, int b, int h, int H, int32_t* labels,
                                    int32_t* perm, vca_stream_t stream);
+
+/* ---- host-buffer pipeline: the end-to-end call of a serving loop ----
+ *
+ * Host-memory plumbing around the paper's operation (no counterpart in the
+ * paper): one call per denoising step of a video model's attention layer.
+ * Each step takes Q, K, V from host memory and returns O to host memory:
+ *   Q, K, V (host) -> the step's staging slot (device)    the pipeline's H2D stream
+ *   vca_vsmooth_prepare_ex, then vca_attention_fp8 (bits 8) or
+ *   vca_attention_nvfp4 (bits 4) on the slot             `stream`
+ *   O (slot) -> o_host                                    the pipeline's D2H stream
+ * Step i uses slot i % slots.  Its input copies start once step i - slots has
+ * finished reading that slot, and its compute once they have landed and step
+ * i - slots's O has been read back.  Copies of later steps and read-backs of
+ * earlier ones therefore overlap the compute.  With slots >= 3 a copy that
+ * stalls is absorbed by the compute of the steps in between.  Page-locked host
+ * memory that sat idle for a while can make the first large copy after the
+ * pause several times slower.  All steps share one state blob, and the compute
+ * runs them in submission order, so a reuse_perm step sees the grouping of the
+ * step before it.
+ *
+ * Memory and resources: `workspace` (device, caller-owned, 256-byte aligned,
+ * at least vca_pipeline_workspace_bytes(...)) holds the state blob, then
+ * `slots` staging sets of Q, K, V and O.  vca_pipeline_create allocates the
+ * pipeline object (host memory), two non-blocking CUDA streams and 3 x slots
+ * events; vca_pipeline_destroy releases them.  These are the only resources
+ * this library creates, and vca_pipeline_wait / vca_pipeline_flush are the
+ * only calls besides vca_get_status that block the host.
+ * Host buffers (bf16 [B,H,N,d] each) should be page-locked; pageable memory
+ * works, but its copies do not overlap.  The step's q/k/v_host must stay
+ * unchanged, and o_host unread, until vca_pipeline_wait(step) (or
+ * vca_pipeline_flush) has returned.
+ * Errors: argument errors are returned before anything is enqueued; a failed
+ * CUDA call returns VCA_ERR_CUDA; device-side failures go to the state blob's
+ * status word, which vca_pipeline_flush reads and clears (vca_get_status
+ * semantics). */
+typedef struct vca_pipeline vca_pipeline;
+
+#define VCA_PIPELINE_MAX_SLOTS 8
+
+/* Workspace bytes for a pipeline of this shape: the state blob rounded up to
+ * 256 bytes, plus `slots` (1..VCA_PIPELINE_MAX_SLOTS) x 4 tensors of
+ * B*H*N*d*2 bytes, each rounded up to 256.  0 for an invalid shape. */
+size_t vca_pipeline_workspace_bytes(int B, int H, int N, int d, int k_clusters, int bits,
+                                    int slots);
+
+/* Create a pipeline over `workspace`.  `stream` carries the compute. */
+int vca_pipeline_create(int B, int H, int N, int d, int k_clusters, int bits, int slots,
+                        void* workspace, size_t workspace_bytes, vca_stream_t stream,
+                        vca_pipeline** out);
+
+/* Option bit of vca_pipeline_submit's flags: run vca_attention_fp8_exp (the
+ * conventional exp-then-cast probability bytes) instead of vca_attention_fp8.
+ * Only for bits = 8. */
+#define VCA_PIPELINE_FP8_EXP 0x100u
+
+/* Enqueue one step.  reuse_perm, iters and seed as for vca_vsmooth_prepare_ex;
+ * flags is VCA_PREP_QK_HADAMARD and/or VCA_PIPELINE_FP8_EXP.  On success *step
+ * (may be NULL) receives the step number, 0, 1, 2, ... in submission order.
+ * Does not block on the GPU. */
+int vca_pipeline_submit(vca_pipeline* p, const void* q_host, const void* k_host,
+                        const void* v_host, void* o_host, int reuse_perm, int iters,
+                        uint64_t seed, unsigned flags, int64_t* step);
+
+/* Block until step `step` (< the number of submitted steps) has written
+ * o_host.  This implies its inputs were read. */
+int vca_pipeline_wait(vca_pipeline* p, int64_t step);
+
+/* Block until every submitted step has finished, then read and clear the
+ * status word of the state blob. */
+int vca_pipeline_flush(vca_pipeline* p);
+
+/* The state blob inside the workspace (device pointer), e.g. for inspection
+ * of the last step's preparation once flushed. */
+void* vca_pipeline_state(vca_pipeline* p);
+
+/* Wait for the pipeline's work, then release its streams, events and the
+ * pipeline object (not the workspace).  NULL is accepted. */
+int vca_pipeline_destroy(vca_pipeline* p);
 
 /* ---- test entry points (device buffers) ---- */
 

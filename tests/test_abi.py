@@ -99,3 +99,35 @@ def test_status_strings(L):
         s = L.vca_status_string(code)
         assert s and s != b"unknown status"
     assert L.vca_status_string(5) == b"unknown status"
+
+
+def test_pipeline_sizes_and_argument_errors(L):
+    """The host-buffer pipeline's workspace size is the state blob plus
+    slots x 4 staging tensors (each rounded to 256 bytes), and create refuses
+    bad arguments before it creates any CUDA resource."""
+    from bit_attention_video_gb300 import vca
+    sb = L.vca_state_bytes(1, 2, 300, 128, 8, 8)
+    t = (1 * 2 * 300 * 128 * 2 + 255) // 256 * 256
+    want = (sb + 255) // 256 * 256 + 3 * 4 * t
+    assert vca.pipeline_workspace_bytes(1, 2, 300, 128, 8, 8, 3) == want
+    assert vca.pipeline_workspace_bytes(1, 2, 300, 128, 8, 8, 0) == 0
+    assert vca.pipeline_workspace_bytes(1, 2, 300, 128, 8, 8, 9) == 0
+    assert vca.pipeline_workspace_bytes(1, 2, 300, 64, 8, 8, 2) == 0
+    fake = C.c_void_p(1 << 20)
+    out = C.c_void_p()
+    create = L.vca_pipeline_create
+    assert create(1, 2, 300, 128, 8, 8, 3, fake, want, None, None) == -1
+    assert create(1, 2, 300, 128, 8, 8, 0, fake, want, None, C.byref(out)) == -1
+    assert create(1, 2, 300, 128, 8, 8, 9, fake, want, None, C.byref(out)) == -1
+    assert create(1, 2, 300, 64, 8, 8, 3, fake, want, None, C.byref(out)) == -2
+    assert create(1, 2, 300, 128, 8, 5, 3, fake, want, None, C.byref(out)) == -2
+    assert create(1, 2, 300, 128, 8, 8, 3, None, want, None, C.byref(out)) == -1
+    assert create(1, 2, 300, 128, 8, 8, 3, C.c_void_p((1 << 20) + 16), want, None,
+                  C.byref(out)) == -1
+    assert create(1, 2, 300, 128, 8, 8, 3, fake, want - 1, None, C.byref(out)) == -4
+    assert not out.value
+    assert L.vca_pipeline_submit(None, fake, fake, fake, fake, 0, 3, 0, 0, None) == -1
+    assert L.vca_pipeline_wait(None, 0) == -1
+    assert L.vca_pipeline_flush(None) == -1
+    assert L.vca_pipeline_destroy(None) == 0
+    assert L.vca_pipeline_state(None) is None
