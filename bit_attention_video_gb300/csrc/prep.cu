@@ -297,7 +297,9 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 // K-major (128-byte swizzle) as the A operand of the first product and
 // MN-major as the A operand of the second; H is stored K-major as H^T.
 // Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
-// warp 1 MMA issuer and TMEM owner; warps 8-11 convert each tile to fp16;
+// warp 1 MMA issuer and TMEM owner; warps 2, 3 and 8-11 convert each tile
+// to fp16 (two converter warps on the sub-partitions without the producer or
+// the issuer);
 // warps 4-7, one token row per thread (the TMEM lane), take each tile's
 // argmin and write its one-hot columns, so converting tile t+1 overlaps the
 // argmin of tile t.  H^T and D_a are double-buffered and X has nx = 3
@@ -320,6 +322,7 @@ enum { KB_XFULL = 0, KB_XEMPTY = KB_XFULL + kPipeStages, KB_XREADY = KB_XEMPTY +
        KB_CNT = KB_UDONE + 3, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
 
 constexpr int kPipeThreads = 384;
+constexpr int kConvThreads = 192;
 __global__ void __launch_bounds__(kPipeThreads, 1)
     kmeans_assign_pipe_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t* cent,
                               int32_t* labels, int32_t* sums, int32_t* counts, int N, int k,
@@ -349,9 +352,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < KB_COUNT; ++i) {
-      const bool workers = (i >= KB_XEMPTY && i < KB_XREADY + 3) ||
-                           (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
-      mbar_init(bar(i), workers ? 128 : 1);
+      const bool conv = i >= KB_XEMPTY && i < KB_XREADY + 3;
+      const bool workers = (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
+      mbar_init(bar(i), conv ? kConvThreads : (workers ? 128 : 1));
     }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -457,9 +460,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar(KB_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 || warp == 2 || warp == 3) {
     // ------------------------------------------------------------ converters
-    const int wt = tid - 256;
+    // six warps: 2, 3 and 8-11.  Conversion step u (32 chunks, two rows)
+    // belongs to converter index u % 6; index 5 (warp 9, beside the MMA
+    // issuer) takes the fewest steps
+    const int ci = warp == 2 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 10 ? 3 : warp == 11 ? 4 : 5;
     bool ok = true;
     for (int t = 0; t < nt && ok; ++t) {
       {
@@ -477,8 +483,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         // and writes the 8 (swizzled) chunks of one 128-byte atom row:
         // no shared-memory bank conflicts
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int i = wt + 128 * u, r = i >> 4, c8 = i & 15;  // row r, channels 8 c8 ..
+        for (int n = 0; n < 11; ++n) {
+          const int u = ci + 6 * n;
+          if (u >= 64) break;
+          const int i = 32 * u + lane, r = i >> 4, c8 = i & 15;  // row r, channels 8 c8 ..
           const uint2 in = *reinterpret_cast<const uint2*>(src + r * 128 + c8 * 8);
           uint32_t w[4];
           i8x4_to_f16x4(in.x, w[0], w[1]);
