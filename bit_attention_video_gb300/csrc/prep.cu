@@ -778,11 +778,15 @@ __device__ __forceinline__ QuotBracket quot_bracket(float s) {
   const float r = __frcp_rn(s);
   return {s, __fmul_rn(r, 1.0f - 0x1p-20f), __fmul_rn(r, 1.0f + 0x1p-20f)};
 }
+// the rare exact path, out of line so that the common one keeps few registers
+__device__ __noinline__ uint32_t e4m3x2_div(float x0, float x1, float s) {
+  return f32x2_to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
 __device__ __forceinline__ uint32_t e4m3x2_quot(float x0, float x1, const QuotBracket& q) {
   const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x0, q.rlo), __fmul_rn(x1, q.rlo));
   const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x0, q.rhi), __fmul_rn(x1, q.rhi));
   if (lo == hi) return lo;
-  return f32x2_to_e4m3x2(__fdiv_rn(x0, q.s), __fdiv_rn(x1, q.s));
+  return e4m3x2_div(x0, x1, q.s);
 }
 
 __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64], float s) {
@@ -799,6 +803,58 @@ __device__ __forceinline__ void store64_e4m3(uint8_t* dst, const float (&f)[64],
       w[e] = lo | (hi << 16);
     }
     d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Eight E4M3 codes (one uint2) of the correctly rounded quotients x / s.
+__device__ __forceinline__ uint2 e4m3x8_quot(const float (&x)[8], const QuotBracket& qb) {
+  return make_uint2(e4m3x2_quot(x[0], x[1], qb) | (e4m3x2_quot(x[2], x[3], qb) << 16),
+                    e4m3x2_quot(x[4], x[5], qb) | (e4m3x2_quot(x[6], x[7], qb) << 16));
+}
+
+// grid (nb, BH), 256 threads, without the rotation: per 128-token block
+// sQ = amax / 448 and Q^ = E4M3(Q / sQ).  Step q (0..7) of thread t covers
+// the 8 values at q * 2048 + 8 t of the block (16 rows per step, each
+// half-warp one whole row), so every load and store instruction of a warp
+// moves one contiguous span; the values stay packed bf16 in registers.
+__global__ void __launch_bounds__(256, 4) quant_q8_rows_kernel(const uint16_t* q, uint8_t* qhat,
+                                                              float* sq, int N, int Npad, int nb,
+                                                              const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, t = threadIdx.x;
+  uint4 w[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int row = j * 128 + u * 16 + t / 16;
+    w[u] = row < N ? *reinterpret_cast<const uint4*>(q + ((size_t)bh * N + row) * 128 + (t % 16) * 8)
+                   : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    m = max3f(m, fabsf(bf_lo(w[u].x)), fabsf(bf_hi(w[u].x)));
+    m = max3f(m, fabsf(bf_lo(w[u].y)), fabsf(bf_hi(w[u].y)));
+    m = max3f(m, fabsf(bf_lo(w[u].z)), fabsf(bf_hi(w[u].z)));
+    m = max3f(m, fabsf(bf_lo(w[u].w)), fabsf(bf_hi(w[u].w)));
+  }
+  const float s = e4m3_scale(block_max(m, red));
+  if (t == 0) sq[(size_t)bh * nb + j] = s;
+  const QuotBracket qb = quot_bracket(s);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int row = j * 128 + u * 16 + t / 16;
+    const float x[8] = {bf_lo(w[u].x), bf_hi(w[u].x), bf_lo(w[u].y), bf_hi(w[u].y),
+                        bf_lo(w[u].z), bf_hi(w[u].z), bf_lo(w[u].w), bf_hi(w[u].w)};
+    *reinterpret_cast<uint2*>(qhat + ((size_t)bh * Npad + row) * 128 + (t % 16) * 8) =
+        e4m3x8_quot(x, qb);
   }
 }
 
@@ -856,6 +912,63 @@ __global__ void key_mean_kernel(const float* ksum, uint16_t* kbar, int N, int nb
   double t = 0.0;
   for (int j = 0; j < nb; ++j) t = __dadd_rn(t, (double)ksum[((size_t)bh * nb + j) * 128 + c]);
   kbar[(size_t)bh * 128 + c] = f32_to_bf16_bits(__double2float_rn(__ddiv_rn(t, (double)N)));
+}
+
+// grid (nb, BH), 256 threads, without the rotation: K' = K[pi] - kbar,
+// per-block E4M3, with the access pattern of quant_q8_rows_kernel (each
+// half-warp gathers one whole row; a thread's 8 channels, and their kbar,
+// are the same in every step).
+__global__ void __launch_bounds__(256, 4) quant_k8_rows_kernel(const uint16_t* k,
+                                                              const int32_t* perm,
+                                                              const uint16_t* kbar, uint8_t* khat,
+                                                              float* sk, int N, int Npad, int nb,
+                                                              const int* status) {
+  __shared__ float red[8];
+  if (prep_skip(status)) return;
+  const int bh = blockIdx.y, j = blockIdx.x, t = threadIdx.x;
+  const uint4 kb = *reinterpret_cast<const uint4*>(kbar + (size_t)bh * 128 + (t % 16) * 8);
+  const float c[8] = {bf_lo(kb.x), bf_hi(kb.x), bf_lo(kb.y), bf_hi(kb.y),
+                      bf_lo(kb.z), bf_hi(kb.z), bf_lo(kb.w), bf_hi(kb.w)};
+  uint4 w[8];
+  bool valid[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int row = j * 128 + u * 16 + t / 16;
+    valid[u] = row < N;
+    if (valid[u]) {
+      const int src = perm[(size_t)bh * N + row];
+      w[u] = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + src) * 128 + (t % 16) * 8);
+    } else {
+      w[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  auto vals = [&](int u, float (&x)[8]) {
+    const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = valid[u] ? __fsub_rn(bf_lo(ww[e]), c[2 * e]) : 0.0f;
+      x[2 * e + 1] = valid[u] ? __fsub_rn(bf_hi(ww[e]), c[2 * e + 1]) : 0.0f;
+    }
+  };
+  float m = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    float x[8];
+    vals(u, x);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) m = max3f(m, fabsf(x[e]), fabsf(x[e + 1]));
+  }
+  const float s = e4m3_scale(block_max(m, red));
+  if (t == 0) sk[(size_t)bh * nb + j] = s;
+  const QuotBracket qb = quot_bracket(s);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int row = j * 128 + u * 16 + t / 16;
+    float x[8];
+    vals(u, x);
+    *reinterpret_cast<uint2*>(khat + ((size_t)bh * Npad + row) * 128 + (t % 16) * 8) =
+        e4m3x8_quot(x, qb);
+  }
 }
 
 // grid (nb, BH), 256 threads: K' = K[pi] - kbar, per-block E4M3.
@@ -1345,9 +1458,16 @@ int launch_prepare8(const PrepArgs& a, cudaStream_t st) {
   uint8_t* mside = S + L.mside;
   float* vamax = reinterpret_cast<float*>(S + L.vamax);
   const int had = (a.flags & VCA_PREP_QK_HADAMARD) ? 1 : 0;
-  quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, had, status);
-  quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, had,
-                                                status);
+  if (had) {
+    // the rotation needs each row in one lane pair
+    quant_q8_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, had, status);
+    quant_k8_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb, had,
+                                                  status);
+  } else {
+    quant_q8_rows_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, qhat, sq, N, Npad, nb, status);
+    quant_k8_rows_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, khat, sk, N, Npad, nb,
+                                                      status);
+  }
   vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
                                               a.reuse != 3 && a.reuse != 4, status);
   vreduce_kernel<<<BH, 256, 0, st>>>(vamax, sv, nb, status);
