@@ -70,3 +70,43 @@ def test_pipeline_refused_submit_and_pageable_memory():
     assert torch.equal(o.view(torch.int16), want[1].view(torch.int16))
     pipe.close()
     pipe.close()                                               # idempotent
+
+
+@pytest.mark.parametrize("qk_hadamard,fp8_exp", [(True, False), (False, True), (True, True)])
+def test_pipeline_flags_match_device_calls(qk_hadamard, fp8_exp):
+    """The pipeline's option bits reach the calls they name: the QK rotation
+    in the preparation, and the conventional exp-then-cast product."""
+    from bit_attention_video_gb300 import vca
+    B, H, N, kc, iters = 1, 2, 600, 8, 2
+    steps = [tuple(_host(x) for x in synth.make_qkv(B, H, N, 128, 8, 300 + i)) for i in range(3)]
+    modes = [0, 1, 0]
+    flags = vca.PREP_QK_HADAMARD if qk_hadamard else 0
+    state = vca.alloc_state(B, H, N, 128, kc, 8)
+    want = []
+    for (q, k, v), m in zip(steps, modes):
+        o = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device="cuda")
+        vca.vsmooth_prepare(q.cuda(), k.cuda(), v.cuda(), kc, state, m, 8, iters, 0, None, flags)
+        (vca.attention_fp8_exp if fp8_exp else vca.attention_fp8)(state, (B, H, N, 128), o)
+        want.append(o.cpu())
+    assert vca.get_status(state) == 0
+    pipe = vca.HostPipeline(B, H, N, 128, k_clusters=kc, bits=8, slots=2, iters=iters,
+                            qk_hadamard=qk_hadamard, fp8_exp=fp8_exp)
+    outs = [torch.empty(B, H, N, 128, dtype=torch.bfloat16).pin_memory() for _ in modes]
+    for s, o, m in zip(steps, outs, modes):
+        pipe.submit(*s, o, reuse_perm=m)
+    pipe.flush()
+    for i, (o, w) in enumerate(zip(outs, want)):
+        assert torch.equal(o.view(torch.int16), w.view(torch.int16)), i
+    pipe.close()
+
+
+def test_pipeline_rejects_exp_product_at_4_bits():
+    from bit_attention_video_gb300 import vca
+    B, H, N = 1, 1, 256
+    q, k, v = (_host(x) for x in synth.make_qkv(B, H, N, 128, 4, 9))
+    o = torch.empty(B, H, N, 128, dtype=torch.bfloat16).pin_memory()
+    pipe = vca.HostPipeline(B, H, N, 128, k_clusters=4, bits=4, slots=2, iters=2, fp8_exp=True)
+    with pytest.raises(vca.VcaError) as e:
+        pipe.submit(q, k, v, o)
+    assert e.value.code == -1
+    pipe.close()
