@@ -764,6 +764,62 @@ __device__ __forceinline__ void hadamard128_pair(float (&f)[64], int h) {
   }
 }
 
+// The same rotation of one row held by a half-warp (lane c8 = lane % 16 holds
+// channels 8 c8 .. 8 c8 + 7): the butterflies of strides 1, 2, 4 inside a
+// lane and 8, 16, 32, 64 across lanes c8 ^ 1, ^ 2, ^ 4, ^ 8 (the lower lane
+// keeps a + b, the upper one a - b), in that order, then the multiply by
+// fp32(1/sqrt(128)): the operations of hadamard128_pair on every value.
+__device__ __forceinline__ void hadamard128_rows(float (&f)[8], int c8) {
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & s) == 0) {
+        const float a = f[i], b = f[i + s];
+        f[i] = __fadd_rn(a, b);
+        f[i + s] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+    const bool upper = (c8 & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, f[i], m);
+      f[i] = upper ? __fsub_rn(o, f[i]) : __fadd_rn(f[i], o);
+    }
+  }
+  constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;  // fp32(1/sqrt(128))
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], kInvSqrt128);
+}
+
+// Step u of a row-mapped block kernel (half-warp = one row, lane c8 = 8
+// channels): the 8 values of row j * 128 + 16 u + t / 16 (0 past N), gathered
+// through perm and centred by kbar (as fp32 words c) when given, rotated
+// when kRot.
+template <bool kRot>
+__device__ __forceinline__ void load_row8(const uint16_t* x, const int32_t* perm, bool centre,
+                                          const float (&c)[8], int bh, int j, int u, int t,
+                                          int N, float (&v)[8]) {
+  const int c8 = t % 16, row = j * 128 + u * 16 + t / 16;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+  if (row < N) {
+    const int src = perm ? perm[(size_t)bh * N + row] : row;
+    const uint4 w = *reinterpret_cast<const uint4*>(x + ((size_t)bh * N + src) * 128 + c8 * 8);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = __uint_as_float(ws[e] << 16);
+      v[2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+    }
+    if (centre)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __fsub_rn(v[e], c[e]);
+  }
+  if constexpr (kRot) hadamard128_rows(v, c8);
+}
+
 // E4M3 codes (RNE, saturating) of the correctly rounded quotients x / s,
 // mostly without dividing.  With r the rounded reciprocal of s, the products
 // x rlo and x rhi (rlo, rhi = r (1 -/+ 2^-20) rounded) carry at most three
@@ -857,6 +913,7 @@ __global__ void __launch_bounds__(256, 4) quant_q8_rows_kernel(const uint16_t* q
         e4m3x8_quot(x, qb);
   }
 }
+
 
 // grid (nb, BH), 256 threads: per 128-token block, sQ = amax / 448 and
 // Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ...
@@ -1145,19 +1202,6 @@ __device__ __forceinline__ uint32_t scale_tile_off(int m, int s) {
   return (uint32_t)(s * 512 + (m % 32) * 16 + (m / 32) * 4);
 }
 
-// 64 values of a row (channels 64h..64h+63): four NVFP4 blocks, 32 code bytes
-// to `dst` and the four scale bytes (one word) to `sdst`.
-__device__ __forceinline__ void store64_nvfp4(const float (&f)[64], float g, uint8_t* dst,
-                                              uint8_t* sdst) {
-  uint32_t sc4 = 0;
-  uint2 pk[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) sc4 |= nvfp4_16(&f[16 * i], g, pk[i]) << (8 * i);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(pk[0].x, pk[0].y, pk[1].x, pk[1].y);
-  d[1] = make_uint4(pk[2].x, pk[2].y, pk[3].x, pk[3].y);
-  *reinterpret_cast<uint32_t*>(sdst) = sc4;
-}
 
 // grid (chunks, BH): max |K - kbar| of each head (the set of K' rows does not
 // depend on the order), as the uint bits of a non-negative float.
@@ -1187,35 +1231,36 @@ __global__ void k4_amax_kernel(const uint16_t* k, const uint16_t* kbar, uint32_t
 }
 
 // grid (nb, BH), 256 threads: max |x H / sqrt(128)| over the rows of a head
-// (x = Q, or K - kbar when kbar is given; the row order does not matter), as
-// the uint bits of a non-negative float: the 4-bit global scales of the
-// rotated operands.
-__global__ void __launch_bounds__(256) rot_amax_kernel(const uint16_t* x, const uint16_t* kbar,
-                                                       uint32_t* amax_bits, int N,
-                                                       const int* status) {
+// (x = Q, or K - kbar when kbar is given), with the row mapping of the
+// block quantisers; as the uint bits of a non-negative float.
+__global__ void __launch_bounds__(256) rot_amax_rows_kernel(const uint16_t* x, const uint16_t* kbar,
+                                                            uint32_t* amax_bits, int N,
+                                                            const int* status) {
   __shared__ float red[8];
   if (prep_skip(status)) return;
-  const int bh = blockIdx.y, j = blockIdx.x;
-  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
-  float f[64];
-  if (row < N) {
-    load64(x + ((size_t)bh * N + row) * 128 + h * 64, f);
-    if (kbar) {
-      const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
+  const int bh = blockIdx.y, j = blockIdx.x, t = threadIdx.x, c8 = t % 16;
+  float c[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  if (kbar) {
+    const uint4 kb = *reinterpret_cast<const uint4*>(kbar + (size_t)bh * 128 + c8 * 8);
+    const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
+    for (int e = 0; e < 4; ++e) {
+      c[2 * e] = __uint_as_float(kw[e] << 16);
+      c[2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
   }
-  hadamard128_pair(f, h);
   float m = 0.0f;
+#pragma unroll 2
+  for (int u = 0; u < 8; ++u) {
+    float v[8];
+    load_row8<true>(x, nullptr, kbar != nullptr, c, bh, j, u, t, N, v);
 #pragma unroll
-  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
+  }
   m = block_max(m, red);
-  if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
+  if (t == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
 }
+
 
 // grid BH, 256 threads: the three global scales gq, gk, gr of a head (gr from
 // the per-block residual channel maxima).
@@ -1236,51 +1281,77 @@ __global__ void g4_kernel(const uint32_t* amax_q, const uint32_t* amax_k, const 
   }
 }
 
-// grid (nb, BH), 256 threads: Q in NVFP4, blocks of 16 along d.  Thread t
-// covers row t/2, channels 64*(t%2) ...
-__global__ void __launch_bounds__(256) quant_q4_kernel(const uint16_t* q, const float* g4,
-                                                       uint8_t* q4, uint8_t* q4s, int N, int Npad,
-                                                       int nb, int hadamard, const int* status) {
-  if (prep_skip(status)) return;
-  const int bh = blockIdx.y, j = blockIdx.x;
-  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
-  float f[64];
-  if (row < N) {
-    load64(q + ((size_t)bh * N + row) * 128 + h * 64, f);
-  } else {
+// Eight values of a 16-element NVFP4 block held by a lane pair (lane parity
+// p holds elements 8p .. 8p+7) under global scale g: the block scale from the
+// pair's maximum, then E2M1 codes of the eight values (value 2i in the low
+// nibble), the same arithmetic as nvfp4_16.  Returns the scale; the whole
+// warp calls it.
+__device__ __forceinline__ uint32_t nvfp4_8_pair(const float (&x)[8], float g, uint32_t& packed) {
+  float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  const uint32_t sc = f32_to_e4m3(__fdiv_rn(m, __fmul_rn(6.0f, g)));
+  const float scv = e4m3_to_f32((uint8_t)sc);
+  uint32_t w = 0u;
+  if (scv > 0.0f) {
+    const float step = __fmul_rn(scv, g);
+    const float r = __frcp_rn(step);
+    const float rlo = __fmul_rn(r, 1.0f - 0x1p-20f), rhi = __fmul_rn(r, 1.0f + 0x1p-20f);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      uint32_t c = f32x2_to_e2m1x2(__fmul_rn(x[i], rlo), __fmul_rn(x[i + 1], rlo));
+      if (c != f32x2_to_e2m1x2(__fmul_rn(x[i], rhi), __fmul_rn(x[i + 1], rhi)))
+        c = f32x2_to_e2m1x2(__fdiv_rn(x[i], step), __fdiv_rn(x[i + 1], step));
+      w |= c << (4 * i);
+    }
   }
-  if (hadamard) hadamard128_pair(f, h);
-  store64_nvfp4(f, g4[bh * 4 + 0], q4 + ((size_t)bh * Npad + row) * 64 + h * 32,
-                q4s + ((size_t)bh * nb + j) * kScaleTileBytes + scale_tile_off(r, h));
+  packed = w;
+  return sc;
 }
 
-// grid (nb, BH), 256 threads: K' = K[pi] - kbar in NVFP4, blocks of 16 along d;
-// scales into the first tile of the block's K'/R scale pair.
-__global__ void __launch_bounds__(256) quant_k4_kernel(const uint16_t* k, const int32_t* perm,
-                                                       const uint16_t* kbar, const float* g4,
-                                                       uint8_t* k4, uint8_t* kr4s, int N,
-                                                       int Npad, int nb, int hadamard,
-                                                       const int* status) {
+// grid (nb, BH), 256 threads, without the rotation: Q (or K' = K[pi] - kbar
+// when perm is given) in NVFP4, blocks of 16 along d.  Step u of thread t
+// covers channels 8 (t % 16) .. +7 of row 16 u + t / 16 of the block, so
+// each half-warp loads one whole row and stores its 64 code bytes; a lane
+// pair holds one 16-element block and the even lane stores its scale.
+template <bool kRot>
+__global__ void __launch_bounds__(256) quant_4_rows_kernel(const uint16_t* x, const int32_t* perm,
+                                                           const uint16_t* kbar, const float* g4,
+                                                           int gidx, uint8_t* codes,
+                                                           uint8_t* scales, size_t scale_stride,
+                                                           int N, int Npad, int nb,
+                                                           const int* status) {
   if (prep_skip(status)) return;
-  const int bh = blockIdx.y, j = blockIdx.x;
-  const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
-  float f[64];
-  if (row < N) {
-    const int src = perm[(size_t)bh * N + row];
-    load64(k + ((size_t)bh * N + src) * 128 + h * 64, f);
-    const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
+  const int bh = blockIdx.y, j = blockIdx.x, t = threadIdx.x, c8 = t % 16;
+  const float g = g4[bh * 4 + gidx];
+  float c[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  if (kbar) {
+    const uint4 kb = *reinterpret_cast<const uint4*>(kbar + (size_t)bh * 128 + c8 * 8);
+    const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-    for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+    for (int e = 0; e < 4; ++e) {
+      c[2 * e] = __uint_as_float(kw[e] << 16);
+      c[2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
+    }
   }
-  if (hadamard) hadamard128_pair(f, h);
-  store64_nvfp4(f, g4[bh * 4 + 1], k4 + ((size_t)bh * Npad + row) * 64 + h * 32,
-                kr4s + ((size_t)bh * nb + j) * 2 * kScaleTileBytes + scale_tile_off(r, h));
+  uint8_t* stile = scales + (size_t)(bh * nb + j) * scale_stride;
+#pragma unroll 2
+  for (int u = 0; u < 8; ++u) {
+    const int m = u * 16 + t / 16, row = j * 128 + m;
+    float v[8];
+    load_row8<kRot>(x, perm, kbar != nullptr, c, bh, j, u, t, N, v);
+    uint32_t pk;
+    const uint32_t sc = nvfp4_8_pair(v, g, pk);
+    *reinterpret_cast<uint32_t*>(codes + ((size_t)bh * Npad + row) * 64 + c8 * 4) = pk;
+    if ((c8 & 1) == 0) {
+      const int b = c8 / 2;  // block 0..7 of the row
+      stile[(b / 4) * 512 + (m % 32) * 16 + (m / 32) * 4 + b % 4] = (uint8_t)sc;
+    }
+  }
 }
+
+
 
 // grid (nb, BH), 256 threads (0..127 own a channel): R = V' - mu in NVFP4,
 // blocks of 16 tokens, written transposed (tokens fastest) with the scales in
@@ -1504,8 +1575,8 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
   const int had = (a.flags & VCA_PREP_QK_HADAMARD) ? 1 : 0;
   if (had) {
-    rot_amax_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, nullptr, amax_q, N, status);
-    rot_amax_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, kbar, amax_k, N, status);
+    rot_amax_rows_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, nullptr, amax_q, N, status);
+    rot_amax_rows_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, kbar, amax_k, N, status);
   } else {
     head_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(q, amax_q, per_head, status);
     k4_amax_kernel<<<dim3(ch, BH), 256, 0, st>>>(kk, kbar, amax_k, per_head, status);
@@ -1513,10 +1584,22 @@ int launch_prepare4(const PrepArgs& a, cudaStream_t st) {
   vpass1_kernel<<<dim3(nb, BH), 256, 0, st>>>(v, perm, mu, vamax, N, nb,
                                               a.reuse != 3 && a.reuse != 4, status);
   g4_kernel<<<BH, 256, 0, st>>>(amax_q, amax_k, vamax, g4, nb, status);
-  quant_q4_kernel<<<dim3(nb, BH), 256, 0, st>>>(q, g4, S + L.q4, S + L.q4s, N, Npad, nb, had,
-                                                status);
-  quant_k4_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, S + L.k4, S + L.kr4s, N, Npad,
-                                                nb, had, status);
+  if (had) {
+    // the rotation needs each row in one lane pair
+    quant_4_rows_kernel<true><<<dim3(nb, BH), 256, 0, st>>>(q, nullptr, nullptr, g4, 0, S + L.q4,
+                                                            S + L.q4s, kScaleTileBytes, N, Npad,
+                                                            nb, status);
+    quant_4_rows_kernel<true><<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, 1, S + L.k4,
+                                                            S + L.kr4s, 2 * kScaleTileBytes, N,
+                                                            Npad, nb, status);
+  } else {
+    quant_4_rows_kernel<false><<<dim3(nb, BH), 256, 0, st>>>(q, nullptr, nullptr, g4, 0, S + L.q4,
+                                                             S + L.q4s, kScaleTileBytes, N, Npad,
+                                                             nb, status);
+    quant_4_rows_kernel<false><<<dim3(nb, BH), 256, 0, st>>>(kk, perm, kbar, g4, 1, S + L.k4,
+                                                             S + L.kr4s, 2 * kScaleTileBytes, N,
+                                                             Npad, nb, status);
+  }
   const int ngroups = (nb + kGroup4 - 1) / kGroup4;
   zero_kernel<<<grid_chunks((size_t)BH * ngroups * kGroup4Bytes / 4, 256, 4096), 256, 0, st>>>(
       reinterpret_cast<uint32_t*>(mside), (size_t)BH * ngroups * kGroup4Bytes / 4);
