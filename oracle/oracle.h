@@ -208,7 +208,10 @@ void orc_attention8_exp(const orc_prep8_out* prep, int N, int d,
                         const int32_t* rows, int nrows, uint16_t* out, double* out64);
 
 /* 4-bit variant: NVFP4 operands, conventional exp, NVFP4 P, means unscaled.
- * parity unpinned beyond the exact-attention error report. */
+ * Pinned: the value path with flat scores; one pass over all keys at the
+ * row maximum when key block 0 holds it; and the unrolled recurrence
+ * (each block quantised at its prefix maximum, weighted by 2^(m_j - M)) on
+ * general inputs, with the formats restated from their definitions. */
 void orc_attention4(const orc_prep4_out* prep, int N, int d,
                     const int32_t* rows, int nrows, uint16_t* out, double* out64);
 

@@ -214,3 +214,133 @@ def test_quantised_attention_against_exact_report(orc, prep8):
     e4 = np.linalg.norm(o4 - ex) / np.linalg.norm(ex)
     print(f"rel L2 vs exact fp64: 8-bit {e8:.4f}, 4-bit {e4:.4f}")
     assert e8 < 0.1 and e4 < 0.4
+
+
+# E2M1 from its definition (1 sign, 2 exponent, 1 mantissa bit, no inf or NaN):
+# the eight magnitudes, code 8 + c the negative of code c
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_val(c):
+    c = np.asarray(c, np.int64)
+    return np.where(c & 8, -1.0, 1.0) * _E2M1[c & 7]
+
+
+def _e2m1_rne(x):
+    """Round non-negative fp32 values to E2M1 magnitudes, nearest with ties to
+    the even code, saturating at 6."""
+    x = np.asarray(x, np.float64)
+    codes = np.zeros(x.shape, np.int64)
+    for i in range(len(_E2M1) - 1):  # choose between code i and i + 1 on [E2M1[i], E2M1[i+1]]
+        lo, hi = _E2M1[i], _E2M1[i + 1]
+        mid = (lo + hi) / 2
+        up = (x > mid) | ((x == mid) & (i % 2 == 1))
+        codes = np.where((x >= lo) & (x <= hi), np.where(up, i + 1, i), codes)
+    return np.where(x > 6.0, 7, codes)
+
+
+@pytest.mark.parametrize("N", [100, 700])
+def test_attention4_single_pass_when_block0_holds_every_row_max(orc, N):
+    """When key block 0 holds each sampled row's largest score, the running
+    maximum of the online recurrence never rises after block 0 (alpha = 1
+    from then on), so the 4-bit output must equal one pass over all keys at
+    the row's global maximum: p = 2^(t - max), P = NVFP4 of 2688 p per 16 keys
+    (UE4M3 scale of the block maximum / 6, E2M1 codes of the quotients),
+    O = (sum_k Pq_k R_k + sum_j r_j mu_j) / sum_k p_k, with r_j and the
+    denominator from the unquantised p (Eq 6 with Appx B's 4-bit operands).
+    The formats are restated here (E2M1 table, UE4M3 through torch's
+    float8_e4m3fn); the permutation is chosen so that block 0 holds the
+    maxima (a K' row's codes do not depend on the order)."""
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 77)
+    q, k, v = q[0, 0], k[0, 0], v[0, 0]
+    rows = np.arange(0, N, 11)
+    log2e = 1.4426950408889634
+
+    def scores(p):
+        d = 128
+        qd = _e2m1_val(p["q4"][rows]) * np.repeat(_e4m3_val(p["q4s"][rows]), 16, 1) * \
+            np.float64(p["gq"][0])
+        kd = _e2m1_val(p["k4"][:N]) * np.repeat(_e4m3_val(p["k4s"][:N]), 16, 1) * \
+            np.float64(p["gk"][0])
+        return qd @ kd.T * (1.0 / np.sqrt(d)) * log2e
+
+    p0 = orc.prepare4(q, k, v, 8, 3, 77)
+    best = p0["perm"][np.argmax(scores(p0), 1)]          # the token holding each row's max
+    first = list(dict.fromkeys(best.tolist()))
+    assert len(first) <= 128
+    perm = np.array(first + [t for t in p0["perm"].tolist() if t not in set(first)], np.int32)
+    p = orc.prepare4(q, k, v, 8, 3, 77, perm=perm)
+    t = scores(p)
+    assert np.all(np.argmax(t, 1) < 128)
+    m = t.max(1, keepdims=True)
+    pr = np.exp2(t - m)                                   # unquantised, max 1
+    npad = (N + 15) // 16 * 16
+    pp = np.zeros((len(rows), npad))
+    pp[:, :N] = pr
+    blocks = pp.reshape(len(rows), -1, 16)
+    amax = (2688.0 * blocks).max(2)
+    scv = _e4m3_val(torch.from_numpy((amax / 6.0).astype(np.float32)).to(torch.float8_e4m3fn)
+                    .view(torch.uint8).numpy())
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x = (2688.0 * blocks / scv[:, :, None]).astype(np.float32)
+    pq = np.where(scv[:, :, None] > 0, _E2M1[_e2m1_rne(x)] * scv[:, :, None] / 2688.0, 0.0)
+    pq = pq.reshape(len(rows), npad)[:, :N]
+    rd = (_e2m1_val(p["r4T"][:, :N]) * np.repeat(_e4m3_val(p["r4s"]), 16, 1)[:, :N] *
+          np.float64(p["gr"][0])).T
+    mu = _f(p["mu"])                                      # [nb][d]
+    nb = mu.shape[0]
+    rj = np.stack([pr[:, j * 128:(j + 1) * 128].sum(1) for j in range(nb)], 1)
+    want = (pq @ rd + rj @ mu) / pr.sum(1, keepdims=True)
+    _, got = orc.attention4(p, rows)
+    assert np.max(np.abs(got - want)) <= 1e-9 * np.max(np.abs(want))
+
+
+def test_attention4_unrolled_recurrence(orc):
+    """The general case: unrolling the online rescaling (the alpha factors
+    telescope), block j's probabilities are taken, and quantised, at the prefix
+    maximum m_j = max of the scores of blocks 0..j, and enter the output with
+    weight 2^(m_j - M), M the row maximum:
+    O = sum_j 2^(m_j - M) (Pq_j R_j + r_j mu_j) / sum_j 2^(m_j - M) r_j."""
+    N = 900
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 91)
+    p = orc.prepare4(q[0, 0], k[0, 0], v[0, 0], 8, 3, 91)
+    rows = np.arange(0, N, 7)
+    log2e = 1.4426950408889634
+    qd = _e2m1_val(p["q4"][rows]) * np.repeat(_e4m3_val(p["q4s"][rows]), 16, 1) * \
+        np.float64(p["gq"][0])
+    kd = _e2m1_val(p["k4"][:N]) * np.repeat(_e4m3_val(p["k4s"][:N]), 16, 1) * \
+        np.float64(p["gk"][0])
+    t = qd @ kd.T * (1.0 / np.sqrt(128)) * log2e
+    rd = (_e2m1_val(p["r4T"][:, :N]) * np.repeat(_e4m3_val(p["r4s"]), 16, 1)[:, :N] *
+          np.float64(p["gr"][0])).T
+    mu = _f(p["mu"])
+    nb = mu.shape[0]
+    bmax = np.stack([t[:, j * 128:(j + 1) * 128].max(1) for j in range(nb)], 1)
+    mj = np.maximum.accumulate(bmax, 1)                     # running maximum after block j
+    M = mj[:, -1:]
+    num = np.zeros((len(rows), 128))
+    den = np.zeros((len(rows), 1))
+    rises = 0
+    for j in range(nb):
+        k0, k1 = j * 128, min(N, (j + 1) * 128)
+        pj = np.exp2(t[:, k0:k1] - mj[:, j:j + 1])
+        pad = np.zeros((len(rows), 128))
+        pad[:, :k1 - k0] = pj
+        blocks = pad.reshape(len(rows), 8, 16)
+        amax = (2688.0 * blocks).max(2)
+        scv = _e4m3_val(torch.from_numpy((amax / 6.0).astype(np.float32)).to(torch.float8_e4m3fn)
+                        .view(torch.uint8).numpy())
+        with np.errstate(divide="ignore", invalid="ignore"):
+            x = (2688.0 * blocks / scv[:, :, None]).astype(np.float32)
+        pq = np.where(scv[:, :, None] > 0, _E2M1[_e2m1_rne(x)] * scv[:, :, None] / 2688.0, 0.0)
+        pq = pq.reshape(len(rows), 128)[:, :k1 - k0]
+        w = np.exp2(mj[:, j:j + 1] - M)
+        rj = pj.sum(1, keepdims=True)
+        num += w * (pq @ rd[k0:k1] + rj * mu[j][None, :])
+        den += w * rj
+        if j > 0:
+            rises += int(np.sum(mj[:, j] > mj[:, j - 1]))
+    assert rises > 0                                         # the rescaling path is exercised
+    want = num / den
+    _, got = orc.attention4(p, rows)
+    assert np.max(np.abs(got - want)) <= 1e-9 * np.max(np.abs(want))
