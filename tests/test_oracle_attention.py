@@ -344,3 +344,49 @@ def test_attention4_unrolled_recurrence(orc):
     want = num / den
     _, got = orc.attention4(p, rows)
     assert np.max(np.abs(got - want)) <= 1e-9 * np.max(np.abs(want))
+
+
+@pytest.mark.parametrize("expcast", [True, False])
+def test_attention8_unrolled_recurrence(orc, expcast):
+    """The 8-bit recurrence unrolled, as for 4 bits: block j's probability
+    bytes are taken at its prefix maximum m_j (Eq 7's ExpCast code
+    clip_[0,120](RNE(8(u+8)+56+beta)), beta = -0.35, or the E4M3 cast of
+    2^(u+8)), and block j enters with weight 2^(m_j - M):
+    O = sv * sum_j 2^(m_j - M) (P_j R^_j + r_j mutilde_j) / sum_j 2^(m_j - M) r_j.
+    The scores are exact (products of E4M3 codes summed in fp64, then the
+    block scales), so the bytes match the oracle's one for one."""
+    N = 900
+    q, k, v = synth.make_qkv(1, 1, N, 128, 8, 92)
+    p = orc.prepare8(q[0, 0], k[0, 0], v[0, 0], 8, 3, 92)
+    rows = np.arange(0, N, 7)
+    log2e, inv = 1.4426950408889634, 1.0 / np.sqrt(128.0)
+    qd = _e4m3_val(p["qhat"][rows])
+    kd = _e4m3_val(p["khat"][:N])
+    rd = _e4m3_val(p["rhatT"][:, :N]).T
+    nb = (N + 127) // 128
+    acc = qd @ kd.T                                          # exact: integers times powers of two
+    sq = p["sq"][rows // 128].astype(np.float64)[:, None]
+    sk = np.repeat(p["sk"].astype(np.float64), 128)[:N][None, :]
+    t = acc * sq * sk * inv * log2e
+    bmax = np.stack([t[:, j * 128:(j + 1) * 128].max(1) for j in range(nb)], 1)
+    mj = np.maximum.accumulate(bmax, 1)
+    M = mj[:, -1:]
+    num = np.zeros((len(rows), 128))
+    den = np.zeros((len(rows), 1))
+    mt = p["mutilde"].astype(np.float64)
+    for j in range(nb):
+        k0, k1 = j * 128, min(N, (j + 1) * 128)
+        u = t[:, k0:k1] - mj[:, j:j + 1]
+        if expcast:
+            code = np.clip(np.rint(8.0 * (u + 8.0) + 56.0 + (-0.35)), 0, 120).astype(np.uint8)
+            w8 = _e4m3_val(code)
+        else:
+            w8 = _e4m3_val(torch.from_numpy(np.exp2(u + 8.0).astype(np.float32))
+                           .to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        w = np.exp2(mj[:, j:j + 1] - M)
+        rj = w8.sum(1, keepdims=True)
+        num += w * (w8 @ rd[k0:k1] + rj * mt[j][None, :])
+        den += w * rj
+    want = p["sv"].astype(np.float64)[None, :] * num / den
+    _, got = orc.attention8(p, rows, expcast=expcast)
+    assert np.max(np.abs(got - want)) <= 1e-9 * np.max(np.abs(want))
