@@ -333,6 +333,9 @@ def run_gpu(args, w):
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     st = att.status()
+    acc_heads = sorted({0, w.H - 1})
+    acc_rows = torch.from_numpy(np.sort(np.random.default_rng(7).choice(w.N, 16, replace=False)))
+    vc_sample = out[0, acc_heads][:, acc_rows.to(out.device)].float().cpu()
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
 
@@ -405,6 +408,21 @@ def run_gpu(args, w):
         bf16_ms = b0.elapsed_time(b1) / nb
         if vca.get_status(None, status) != 0:
             bf16_ms = None
+        bf16_sample = out[0, acc_heads][:, acc_rows.to(out.device)].float().cpu()
+    else:
+        bf16_sample = None
+
+    # relative L2 of the sampled output rows against exact attention in fp64
+    # (softmax(Q K^T / sqrt(d)) V on the host inputs)
+    def rel_l2_vs_exact(sample):
+        num = den = 0.0
+        for i, h in enumerate(acc_heads):
+            qh, kh, vh = (x[0, h].to(torch.float64) for x in host)
+            s_ = (qh[acc_rows] @ kh.T) / np.sqrt(w.d)
+            ex = torch.softmax(s_, dim=1) @ vh
+            num += float(((sample[i].to(torch.float64) - ex) ** 2).sum())
+            den += float((ex ** 2).sum())
+        return (num / den) ** 0.5
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -451,6 +469,11 @@ def run_gpu(args, w):
         "gpu_launches": launches_per_step(grouping_iters(args), not groups(args), w.bits)
         * args.steps,
         "clocks": clocks.summary(),
+        "accuracy": {"rel_l2_vs_fp64_exact": rel_l2_vs_exact(vc_sample),
+                     "bf16_ref_rel_l2_vs_fp64_exact":
+                         rel_l2_vs_exact(bf16_sample) if bf16_sample is not None else None,
+                     "rows": f"16 sampled query rows of heads {acc_heads} (batch 0), the last "
+                             "timed step's output; exact attention in fp64 on the host inputs"},
     }
     if dist:
         dist.barrier()

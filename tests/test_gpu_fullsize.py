@@ -1,7 +1,9 @@
 """GPU: the full Wan2.2-like 720p workload (B=1, H=40, N=75600, k=64, 10
 iterations) in the launch configuration the benchmark times, at 8 and 4 bits;
 preparation of two sampled heads is bit-exact with the oracle and sampled
-attention rows are within relative L2 2e-3 (8-bit) and 1e-2 (4-bit)."""
+attention rows are within relative L2 2e-3 (8-bit) and 1e-2 (4-bit) of the
+oracle; their error against exact fp64 attention is reported and bounded
+loosely (0.1 and 0.4, the bounds of the oracle's own report)."""
 import numpy as np
 import pytest
 import torch
@@ -36,8 +38,11 @@ def test_wan720p_sampled_parity(orc):
         _, ref = orc.attention8(p, rows)
         got = bf16_f64(to_np_u16(out[0, h][torch.from_numpy(rows).cuda()]))
         err = rel_l2(got, ref)
-        print(f"head {h}: relative L2 vs oracle {err:.2e}")
+        ex = orc.attention_exact(q[0, h], k[0, h], v[0, h], rows)
+        ex_err = rel_l2(got, ex)
+        print(f"head {h}: relative L2 vs oracle {err:.2e}, vs exact fp64 attention {ex_err:.3f}")
         assert err <= 2e-3
+        assert ex_err < 0.1
 
 
 def test_wan720p_nvfp4_sampled_parity(orc):
@@ -62,5 +67,8 @@ def test_wan720p_nvfp4_sampled_parity(orc):
         _, ref = orc.attention4(p, rows)
         got = bf16_f64(to_np_u16(out[0, h][torch.from_numpy(rows).cuda()]))
         err = rel_l2(got, ref)
-        print(f"head {h}: 4-bit relative L2 vs oracle {err:.2e}")
+        ex = orc.attention_exact(q[0, h], k[0, h], v[0, h], rows)
+        ex_err = rel_l2(got, ex)
+        print(f"head {h}: 4-bit relative L2 vs oracle {err:.2e}, vs exact fp64 attention {ex_err:.3f}")
         assert err <= 1e-2
+        assert ex_err < 0.4
