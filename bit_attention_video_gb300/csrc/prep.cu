@@ -1108,9 +1108,10 @@ __global__ void vreduce_kernel(const float* vamax, float* sv, int nb, const int*
   if (half == 0) sv[(size_t)bh * 128 + c] = e4m3_scale(fmaxf(part[0][c], part[1][c]));
 }
 
-// grid (nb, BH), 256 threads (0..127 own a channel): R = V' - mu, R^ =
-// E4M3(R / sv) written transposed (tokens fastest); mutilde = mu / sv and the
-// mean operand of the restoration MMA.  Blocks form groups of kGroup aligned
+// grid (nb, BH), 256 threads (threads t and t + 128 share channel t % 128,
+// 64 tokens each): R = V' - mu, R^ = E4M3(R / sv) written transposed (tokens
+// fastest) through a swizzled shared tile, so each channel's 128 codes leave
+// as one line; mutilde = mu / sv and the mean operand of the restoration MMA.  Blocks form groups of kGroup aligned
 // to the last block (block j is slot (j + gpad) % kGroup of group
 // (j + gpad) / kGroup); per group two 128 (channel) x 16 (K) bf16 K-major
 // chunks without swizzle, element (c, k) at (c/8)*256 + (k/8)*128 + (c%8)*16
@@ -1123,31 +1124,42 @@ __global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const in
                                                      uint8_t* mside, int N, int Npad, int nb,
                                                      int ngroups, int gpad, const int* status) {
   __shared__ __align__(16) uint16_t tile[128][128];
+  __shared__ __align__(16) uint8_t codes[128 * 128];  // [channel][token], 16-byte chunks swizzled
   if (prep_skip(status)) return;
-  const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  const int bh = blockIdx.y, j = blockIdx.x;
+  // threads t and t + 128 share channel c = t % 128, tokens 64 hh .. 64 hh + 63
+  const int c = threadIdx.x % 128, hh = threadIdx.x / 128;
   gather_block(v, perm, bh, j, N, tile);
   __syncthreads();
-  if (c >= 128) return;
   const size_t o = ((size_t)bh * nb + j) * 128 + c;
   const float mf = bf16_bits_to_f32(mu[o]);
   const float s = sv[(size_t)bh * 128 + c];
   const QuotBracket qb = quot_bracket(s);
-  uint4* dst = reinterpret_cast<uint4*>(rhatT + ((size_t)bh * 128 + c) * Npad + (size_t)j * 128);
 #pragma unroll 2
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float y[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int r = q * 16 + e * 4 + u;
+        const int r = hh * 64 + q * 16 + e * 4 + u;
         y[u] = (j * 128 + r < N) ? __fsub_rn(bf16_bits_to_f32(tile[r][c]), mf) : 0.0f;
       }
       w[e] = e4m3x2_quot(y[0], y[1], qb) | (e4m3x2_quot(y[2], y[3], qb) << 16);
     }
-    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    const int chunk = (hh * 4 + q) ^ (c & 7);
+    *reinterpret_cast<uint4*>(codes + c * 128 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  __syncthreads();
+  // each group of 8 threads stores one channel's 128 codes as one line
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = threadIdx.x + 256 * k, cc = i / 8, ch = i % 8;
+    const uint4 w = *reinterpret_cast<const uint4*>(codes + cc * 128 + ((ch ^ (cc & 7)) * 16));
+    *reinterpret_cast<uint4*>(rhatT + ((size_t)bh * 128 + cc) * Npad + (size_t)j * 128 + ch * 16) = w;
+  }
+  if (hh != 0) return;
   const float mt = __fdiv_rn(mf, s);
   mutilde[o] = mt;
   const uint16_t hi = f32_to_bf16_bits(mt);
