@@ -945,18 +945,25 @@ __device__ __forceinline__ float tree128(float (&v)[128]) {
   return v[0];
 }
 
-// grid (nb, BH), 128 threads (one per channel): fp32 tree sum of each block of
-// the original key order.
-__global__ void __launch_bounds__(128) key_block_sum_kernel(const uint16_t* k, float* ksum, int N,
+// grid (nb, BH), 256 threads: fp32 tree sum of each block of the original key
+// order.  The block is staged in shared memory with coalesced 16-byte loads
+// of whole rows (zero rows past N); threads 0..127 then sum one channel each.
+__global__ void __launch_bounds__(256) key_block_sum_kernel(const uint16_t* k, float* ksum, int N,
                                                             int nb, const int* status) {
+  __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+    const int r = i / 16, c16 = i % 16, row = j * 128 + r;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (row < N) w = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + row) * 128 + c16 * 8);
+    *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = w;
+  }
+  __syncthreads();
+  if (c >= 128) return;
   float v[128];
 #pragma unroll
-  for (int r = 0; r < 128; ++r) {
-    const int row = j * 128 + r;
-    v[r] = row < N ? bf16_bits_to_f32(k[((size_t)bh * N + row) * 128 + c]) : 0.0f;
-  }
+  for (int r = 0; r < 128; ++r) v[r] = bf16_bits_to_f32(tile[r][c]);
   ksum[((size_t)bh * nb + j) * 128 + c] = tree128(v);
 }
 
@@ -1513,7 +1520,7 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
     return VCA_OK;
   }
   float* ksum = reinterpret_cast<float*>(S + L.ksum);
-  key_block_sum_kernel<<<dim3(nb, BH), 128, 0, st>>>(kk, ksum, N, nb, status);
+  key_block_sum_kernel<<<dim3(nb, BH), 256, 0, st>>>(kk, ksum, N, nb, status);
   key_mean_kernel<<<BH, 128, 0, st>>>(ksum, kbar, N, nb, status);
   return VCA_OK;
 }
