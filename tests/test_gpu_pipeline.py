@@ -34,9 +34,9 @@ def _direct(steps, B, H, N, kc, bits, iters, modes):
     (8, 1, [0, 1, 0]),
     (4, 2, [0, 1, 2, 0]),
 ])
-def test_pipeline_matches_device_calls(bits, slots, modes):
+def test_pipeline_matches_device_calls(bits, slots, modes, B=1, H=2, N=700):
     from bit_attention_video_gb300 import vca
-    B, H, N, kc, iters = 1, 2, 700, 8, 3
+    kc, iters = 8, 3
     steps = [tuple(_host(x) for x in synth.make_qkv(B, H, N, 128, 8, 100 + i))
              for i in range(len(modes))]
     want = _direct(steps, B, H, N, kc, bits, iters, modes)
@@ -50,6 +50,11 @@ def test_pipeline_matches_device_calls(bits, slots, modes):
     for i, (o, w) in enumerate(zip(outs, want)):
         assert torch.equal(o.view(torch.int16), w.view(torch.int16)), i
     pipe.close()
+
+
+def test_pipeline_batch_of_two_ragged_length():
+    """B = 2 and a length that is not a multiple of 128."""
+    test_pipeline_matches_device_calls(8, 3, [0, 1, 0, 2], B=2, H=1, N=333)
 
 
 def test_pipeline_refused_submit_and_pageable_memory():
