@@ -266,7 +266,10 @@ int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters, 
  * Errors: argument errors are returned before anything is enqueued; a failed
  * CUDA call returns VCA_ERR_CUDA; device-side failures go to the state blob's
  * status word, which vca_pipeline_flush reads and clears (vca_get_status
- * semantics). */
+ * semantics).
+ * Threads: a pipeline object is not thread-safe; one host thread at a time
+ * calls submit, wait and flush on it.  Separate pipelines (separate
+ * workspaces) may run from separate threads. */
 typedef struct vca_pipeline vca_pipeline;
 
 #define VCA_PIPELINE_MAX_SLOTS 8
