@@ -509,7 +509,7 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=30,
+    ap.add_argument("--e2e-steps", type=int, default=60,
                     help="steps per timed end-to-end run (the pipeline fills and drains once per run)")
     args = ap.parse_args()
     if args.reuse + args.warm + args.plain + args.naive > 1:
