@@ -69,6 +69,7 @@ def check_head4(g, p, bh, N, what=("labels", "perm", "centroids")):
     (2, 1, 300, 4, 8, 3),        # B > 1, three blocks
     (1, 1, 128, 4, 4, 2),        # exactly one block
     (1, 3, 1, 1, 1, 1),          # one token
+    (1, 1, 700, 32, 96, 2),      # 64 < k <= 128 at 4 bits
 ])
 def test_prepare4_bit_exact(orc, B, H, N, C, kc, iters):
     seed = 0xC0FFEE + N

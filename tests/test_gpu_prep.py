@@ -67,6 +67,7 @@ def check_head8(g, p, bh, N, what=("labels", "perm", "centroids")):
     (1, 1, 2500, 64, 200, 2),    # k > 96 (single accumulator group), several sort chunks
     (1, 2, 1300, 64, 96, 3),     # 64 < k <= 128: the tensor-core Lloyd step, two D_a chunks
     (1, 1, 700, 24, 24, 3),      # 16 < k <= 32: one 32-column D_a load
+    (1, 1, 1100, 64, 256, 2),    # the largest k (CUDA-core assignment, one accumulator group)
 ])
 def test_prepare8_bit_exact(orc, B, H, N, C, kc, iters):
     seed = 0xC0FFEE + N
