@@ -160,29 +160,41 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
 
 // grid BH, 128 threads: initial centroids = features of k distinct tokens drawn
 // by SplitMix64 from seed ^ (0x9E3779B97F4A7C15 * (bh + 1)); zero the sums.
+// Warp 0 draws: every lane steps the same generator, the lanes test the
+// candidate against a share of the accepted indices each, and a candidate
+// is accepted when no lane finds it (the draws and acceptances of a single
+// thread testing them in turn).  The k rows are then copied in 16-byte
+// chunks (d = 128).
 __global__ void kmeans_init_kernel(const int8_t* x, int8_t* cent, int32_t* sums, int32_t* counts,
                                    uint64_t seed, int N, int k, int d, int* status) {
   __shared__ int32_t idx[256];
   if (prep_skip(status)) return;
-  const int bh = blockIdx.x;
-  if (threadIdx.x == 0) {
+  const int bh = blockIdx.x, lane = threadIdx.x % 32;
+  if (threadIdx.x < 32) {
     uint64_t st = seed ^ (0x9E3779B97F4A7C15ull * (uint64_t)(bh + 1));
     int have = 0;
     // k <= N distinct draws; the bound only guards against a corrupted k
     for (long long tries = 0; have < k && tries < (1ll << 26); ++tries) {
       const int32_t cand = (int32_t)(splitmix64_next(st) % (uint64_t)N);
       bool dup = false;
-      for (int i = 0; i < have; ++i) dup |= (idx[i] == cand);
-      if (!dup) idx[have++] = cand;
+      for (int i = lane; i < have; i += 32) dup |= (idx[i] == cand);
+      if (!__any_sync(0xffffffffu, dup)) {
+        if (lane == 0) idx[have] = cand;
+        ++have;
+        __syncwarp();
+      }
     }
-    if (have < k) atomicOr(status, kStatBadArg);
+    if (lane == 0 && have < k) atomicOr(status, kStatBadArg);
   }
   __syncthreads();
-  for (int m = 0; m < k; ++m)
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      cent[((size_t)bh * k + m) * d + c] = x[((size_t)bh * N + idx[m]) * d + c];
-      sums[((size_t)bh * k + m) * d + c] = 0;
-    }
+  const int chunks = d / 16;
+  for (int i = threadIdx.x; i < k * chunks; i += blockDim.x) {
+    const int m = i / chunks, c16 = i % chunks;
+    reinterpret_cast<uint4*>(cent + ((size_t)bh * k + m) * d)[c16] =
+        reinterpret_cast<const uint4*>(x + ((size_t)bh * N + idx[m]) * d)[c16];
+  }
+  int4* s4 = reinterpret_cast<int4*>(sums + (size_t)bh * k * d);
+  for (int i = threadIdx.x; i < k * d / 4; i += blockDim.x) s4[i] = make_int4(0, 0, 0, 0);
   for (int m = threadIdx.x; m < k; m += blockDim.x) counts[(size_t)bh * k + m] = 0;
 }
 
