@@ -926,9 +926,10 @@ __global__ void __launch_bounds__(256, 4) quant_q8_rows_kernel(const uint16_t* q
   }
 }
 
-
 // grid (nb, BH), 256 threads: per 128-token block, sQ = amax / 448 and
-// Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ...
+// Q^ = E4M3(Q / sQ).  Thread t covers row t/2, channels 64*(t%2) ..., so a
+// lane pair holds the row that hadamard128_pair rotates: the launch path of
+// the QK rotation (quant_q8_rows_kernel serves the unrotated one).
 __global__ void __launch_bounds__(256, 3) quant_q8_kernel(const uint16_t* q, uint8_t* qhat, float* sq,
                                                        int N, int Npad, int nb, int hadamard,
                                                        const int* status) {
@@ -1047,7 +1048,9 @@ __global__ void __launch_bounds__(256, 4) quant_k8_rows_kernel(const uint16_t* k
   }
 }
 
-// grid (nb, BH), 256 threads: K' = K[pi] - kbar, per-block E4M3.
+// grid (nb, BH), 256 threads: K' = K[pi] - kbar, per-block E4M3, a lane pair
+// per row as in quant_q8_kernel (the QK rotation's launch path;
+// quant_k8_rows_kernel serves the unrotated one).
 __global__ void __launch_bounds__(256, 3) quant_k8_kernel(const uint16_t* k, const int32_t* perm,
                                                        const uint16_t* kbar, uint8_t* khat,
                                                        float* sk, int N, int Npad, int nb,
