@@ -98,12 +98,6 @@ enum { B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = B_KVFULL + kStages, B_SFULL = B_KV
        B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2,
        B_DRAIN = B_PVDONE + 2, B_COUNT = B_DRAIN + 1 };
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -397,25 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bar(B_SFREE + X));
-      if (j == nb - 1 && valid_last < 128) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= valid_last) s[c] = 0xFF800000u;  // -inf: masked key -> byte 0
-      }
-      // row maximum (eight chains of three-input max)
-      float m8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-#pragma unroll
-      for (int c = 16; c < 128; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          m8[i] = max3(m8[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-      const float mx = fmaxf(fmaxf(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5])),
-                             fmaxf(m8[6], m8[7]));
-      const float Mn = fmaxf(M, a * mx);
+      if (j == nb - 1 && valid_last < 128) mask_tail128(s, valid_last);  // masked keys: byte 0
+      const float Mn = fmaxf(M, a * row_max128(s));
       const float alpha = ex2((M - Mn) * 0.125f);  // 0 on the first block
-      const float b = kExpCastBias - Mn;
       // ExpCast bytes, four per 32-bit TMEM column (the A layout of the
       // product: byte k of column c is key 4c + k)
       uint32_t w[32];
@@ -430,21 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p3 = ex2(fmaf(__uint_as_float(s[c + 3]), a8, b8));
           w[c / 4] = f32x4_to_e4m3x4(p0, p1, p2, p3);
         }
-      } else if (expcast_fast_is_exact(Mn)) {
-        const float a128 = a * 0.0078125f, b128 = b * 0.0078125f;
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          const uint2 e0 = expcast_pair_bits(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), a128, b128);
-          const uint2 e1 = expcast_pair_bits(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), a128, b128);
-          w[c / 4] = __byte_perm(__byte_perm(e0.x, e0.y, 0x0040), __byte_perm(e1.x, e1.y, 0x0040), 0x5410);
-        }
       } else {
-#pragma unroll
-        for (int c = 0; c < 128; c += 4)
-          w[c / 4] = expcast_code(__uint_as_float(s[c]), a, b) |
-                     (expcast_code(__uint_as_float(s[c + 1]), a, b) << 8) |
-                     (expcast_code(__uint_as_float(s[c + 2]), a, b) << 16) |
-                     (expcast_code(__uint_as_float(s[c + 3]), a, b) << 24);
+        expcast_row_bytes(s, a, Mn, w);
       }
       if (j > 0) {
         // the previous product read P^ and wrote the accumulator

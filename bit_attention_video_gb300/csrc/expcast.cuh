@@ -35,8 +35,72 @@ __device__ __forceinline__ uint2 expcast_pair_bits(float acc0, float acc1, float
   return make_uint2((uint32_t)out, (uint32_t)(out >> 32));
 }
 
-// With M the running maximum (scaled by 8, log2 domain), the fast form needs
-// no upper clip when t = fma(a, acc, 119.65 - M) provably stays below 120.5.
-__device__ __forceinline__ bool expcast_fast_is_exact(float M) { return fabsf(M) < 1048576.0f; }
+// When the pair form gives exactly the reference form's byte, for scores with
+// a * acc <= M (M the running maximum, scaled by 8, log2 domain):
+//   - |M| < 2^20: t = fma(a, acc, 119.65 - M) stays below 120.5 (the rounding
+//     of a * max and of 119.65 - M each add at most 2^-4), so the upper clip
+//     never acts;
+//   - a = 0 or a >= 2^-119: a * 2^-7 is exact (not subnormal).  (b * 2^-7 is
+//     always exact: 119.65 - M is 0 or at least 2^-18 in magnitude.)
+__device__ __forceinline__ bool expcast_fast_is_exact(float M, float a) {
+  return fabsf(M) < 1048576.0f && (a == 0.0f || a >= 1.50463277e-36f /* 2^-119 */);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of a row's 128 scores (fp32 bit patterns): eight chains of
+// three-input max.  NaN scores are ignored (max.f32 returns the other operand).
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    m8[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      m8[i] = fmax3(m8[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+  return fmaxf(fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5])),
+               fmaxf(m8[6], m8[7]));
+}
+
+// The ExpCast bytes of one row of a 128-key block relative to the running
+// maximum Mn (>= a * every score), four per word in the A-operand layout of
+// the value product (byte k of word c is key 4c + k).  The pair form when it
+// is exact, else the reference form.
+__device__ __forceinline__ void expcast_row_bytes(const uint32_t (&s)[128], float a, float Mn,
+                                                  uint32_t (&w)[32]) {
+  const float b = kExpCastBias - Mn;
+  if (expcast_fast_is_exact(Mn, a)) {
+    const float a128 = a * 0.0078125f, b128 = b * 0.0078125f;
+#pragma unroll
+    for (int c = 0; c < 128; c += 4) {
+      const uint2 e0 = expcast_pair_bits(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), a128,
+                                         b128);
+      const uint2 e1 = expcast_pair_bits(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]),
+                                         a128, b128);
+      w[c / 4] = __byte_perm(__byte_perm(e0.x, e0.y, 0x0040), __byte_perm(e1.x, e1.y, 0x0040),
+                             0x5410);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 128; c += 4)
+      w[c / 4] = expcast_code(__uint_as_float(s[c]), a, b) |
+                 (expcast_code(__uint_as_float(s[c + 1]), a, b) << 8) |
+                 (expcast_code(__uint_as_float(s[c + 2]), a, b) << 16) |
+                 (expcast_code(__uint_as_float(s[c + 3]), a, b) << 24);
+  }
+}
+
+// Keys at and past `valid` of the last block are masked: score -inf, byte 0.
+__device__ __forceinline__ void mask_tail128(uint32_t (&s)[128], int valid) {
+#pragma unroll
+  for (int c = 0; c < 128; ++c)
+    if (c >= valid) s[c] = 0xFF800000u;
+}
 
 }  // namespace vca

@@ -1,5 +1,6 @@
-"""GPU: the ExpCast device function and the format encoders are bit-exact with
-the oracle; every tcgen05 operand layout the kernels use multiplies correctly."""
+"""GPU: the ExpCast device function (its reference form, and the per-row form
+the 8-bit attention kernel runs) and the format encoders are bit-exact with the
+oracle; every tcgen05 operand layout the kernels use multiplies correctly."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +35,96 @@ def test_expcast_device_function_bit_exact(V, orc):
     got = out.cpu().numpy()
     bad = np.nonzero(got != ref)[0]
     assert bad.size == 0, f"{bad.size} mismatches, first at {bad[:5]}: {got[bad[:5]]} vs {ref[bad[:5]]}"
+
+
+def _expcast_rows_inputs():
+    """Rows of 128 raw scores with the kernel's per-row scale a and previous
+    running maximum M: random rows (first block, no rise, rise), exact
+    rounding ties of the FMA, both clip ends, masked tails, NaN scores, |M|
+    on both sides of 2^20 (where the kernel switches between its two forms)
+    and beyond, and subnormal a * 2^-7."""
+    rng = np.random.default_rng(31)
+    R = 8192
+    s = np.zeros((R, 128), np.float32)
+    a = np.ones(R, np.float32)
+    M = np.full(R, -np.inf, np.float32)
+    valid = np.full(R, 128, np.int32)
+    # random rows: a * s spans tens to hundreds below the maximum
+    n = 4096
+    a[:n] = (10.0 ** rng.uniform(-4, 0.5, n)).astype(np.float32)
+    sig = rng.uniform(1, 60, n) / a[:n]
+    s[:n] = (rng.standard_normal((n, 128)) * sig[:, None]).astype(np.float32)
+    am = (a[:n] * s[:n].max(1)).astype(np.float32)
+    kind = rng.integers(0, 3, n)
+    M[:n] = np.where(kind == 0, -np.inf, np.where(kind == 1, am + rng.uniform(0, 50, n),
+                                                    am - rng.uniform(0, 50, n))).astype(np.float32)
+    # exact ties: b = 119.65f - M = 100 exactly, a s = t - 100 with t = k + 1/2
+    r0, r1 = 4096, 4608
+    M[r0:r1] = np.float32(np.float32(119.65) - np.float32(100))
+    t = rng.integers(-3, 120, (r1 - r0, 128)) + 0.5
+    a[r0:r1] = np.where(np.arange(r1 - r0) % 2 == 0, 1.0, 0.5).astype(np.float32)
+    s[r0:r1] = ((t - 100) / a[r0:r1, None]).astype(np.float32)
+    # both clip ends: t in (-1, 1) and the row maximum at 119.65
+    r0, r1 = 4608, 4864
+    M[r0:r1] = np.float32(np.float32(119.65) - np.float32(100))
+    s[r0:r1] = rng.uniform(-101, -99, (r1 - r0, 128)).astype(np.float32)
+    s[r0:r1, 0] = M[r0:r1]
+    # masked tails and NaN scores
+    r0, r1 = 4864, 5376
+    s[r0:r1] = (rng.standard_normal((r1 - r0, 128)) * 30).astype(np.float32)
+    valid[r0:r1] = rng.integers(1, 128, r1 - r0)
+    s[r0 + 1::7, 5] = np.nan
+    M[r0:r1:3] = np.float32(5.0)
+    # |M| around 2^20 and beyond (a s within 200 of M)
+    r0, r1 = 5376, 6400
+    base = np.array([2 ** 20 - 1, 2 ** 20 - 0.5, 2 ** 20, 2 ** 20 + 1, 2 ** 21, 2 ** 23, 2 ** 24 + 2,
+                     3 * 2 ** 24, 2 ** 30, -(2 ** 20) + 1, -(2 ** 20), -(2 ** 20) - 8, -(2 ** 24)],
+                    np.float64)
+    pick = base[rng.integers(0, base.size, r1 - r0)]
+    a[r0:r1] = rng.choice(np.array([1.0, 3.0, 0.7, 0.125], np.float32), r1 - r0)
+    s[r0:r1] = ((pick[:, None] - rng.uniform(0, 200, (r1 - r0, 128))) / a[r0:r1, None]) \
+        .astype(np.float32)
+    s[r0:r1, 7] = (pick / a[r0:r1]).astype(np.float32)
+    M[r0:r1] = np.where(rng.integers(0, 2, r1 - r0) == 0, -np.inf, pick).astype(np.float32)
+    # a below 2^-119 (a * 2^-7 subnormal: the single-FMA form) and just at it
+    r0, r1 = 6400, 6656
+    a[r0:r1] = rng.choice(np.array([2.0 ** -121, 2.0 ** -120, 2.0 ** -119, 2.0 ** -118],
+                                   np.float32), r1 - r0)
+    s[r0:r1] = (rng.uniform(-100, 0, (r1 - r0, 128)) / a[r0:r1, None]).astype(np.float32)
+    # the rest: ordinary rows with small scales
+    r0 = 6656
+    a[r0:] = np.float32(0.05)
+    s[r0:] = (rng.standard_normal((R - r0, 128)) * 400).astype(np.float32)
+    return s, a, M, valid
+
+
+def test_expcast_kernel_form_bit_exact(V, orc):
+    """The softmax step the 8-bit attention kernel runs (paper §3.3 Eq 7 with
+    the running maximum of Eq 1): the paired 1/128-scaled FMA with the
+    1.5 x 2^16 rounding add where it is exact, the single-FMA form elsewhere,
+    byte for byte against the oracle's single-FMA fp32 form, on 2^20 scores."""
+    s, a, M, valid = _expcast_rows_inputs()
+    R = s.shape[0]
+    codes = torch.empty((R, 128), dtype=torch.uint8, device="cuda")
+    Mn = torch.empty(R, dtype=torch.float32, device="cuda")
+    V.debug_expcast_rows(torch.from_numpy(s).cuda(), torch.from_numpy(a).cuda(),
+                         torch.from_numpy(M).cuda(), torch.from_numpy(valid).cuda(), codes, Mn)
+    got, got_mn = codes.cpu().numpy(), Mn.cpu().numpy()
+    # the running maximum and the bytes the oracle gives for it
+    sm = s.copy()
+    sm[np.arange(128)[None, :] >= valid[:, None]] = -np.inf
+    with np.errstate(invalid="ignore", over="ignore"):
+        mn = np.fmax(M, (a * np.nanmax(sm, axis=1)).astype(np.float32))
+        b = (np.float32(119.65) - mn).astype(np.float32)
+    assert np.array_equal(got_mn, mn), f"running max differs in {np.sum(got_mn != mn)} rows"
+    ref = orc.expcast_f32(sm.ravel(), np.repeat(a, 128), np.repeat(b, 128)).reshape(R, 128)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, (f"{len(bad)} bytes differ, first rows {bad[:5, 0]}: "
+                           f"{got[tuple(bad[:5].T)]} vs {ref[tuple(bad[:5].T)]}")
+    # the inputs reach what they are meant to: ties, both clips, both forms
+    assert np.sum(ref == 120) >= R // 2 and np.sum(ref == 0) > 10000
+    big = np.abs(mn) >= 2 ** 20
+    assert 100 < np.sum(big) < R - 100
 
 
 def test_encoders_bit_exact(V, orc):
