@@ -16,6 +16,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvca.so")
+# The debug build: the same sources with -DVCA_DEBUG, whose kernels check the
+# data-dependent indices they address memory with (a cached permutation, a
+# label) and record an error instead of reading or writing out of bounds.
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libvca.so")
 SOURCES = ["api.cu", "prep.cu", "attn_fp8.cu", "attn_bf16.cu", "attn_nvfp4.cu", "debug.cu",
            "pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -42,17 +47,20 @@ def _stale(target, inputs) -> bool:
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile libvca.so (debug=True: the -DVCA_DEBUG build in its own folder)."""
+    out_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     deps = _deps()
     objs, jobs = [], []
+    flags = FLAGS + (["-DVCA_DEBUG"] if debug else [])
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + deps):
-            jobs.append([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *ARCH, *flags, "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -62,18 +70,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         for src, log in ex.map(run, jobs):
-            with open(os.path.join(BUILD, os.path.basename(src) + ".ptxas.txt"), "w") as f:
+            with open(os.path.join(out_dir, os.path.basename(src) + ".ptxas.txt"), "w") as f:
                 f.write(log)
             if verbose:
                 print(log)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True,
                            text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -197,9 +197,11 @@ int vca_get_status(void* state, int* status_word, vca_stream_t stream) {
     vca_state_layout L;
     compute_layout(1, 1, 1, 128, 1, 8, &L);  // the status offset does not depend on the shape
     dev = reinterpret_cast<int*>((uint8_t*)state + L.status);
+  } else if (!status_word) {
+    dev = noalloc_status_word();  // the allocation-free grouping call's word
   }
-  if (!dev) return VCA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return VCA_ERR_CUDA;
+  if (!dev) return VCA_OK;  // that call has not run on this device
   int h = 0;
   if (cudaMemcpy(&h, dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return VCA_ERR_CUDA;
   const int zero = 0;

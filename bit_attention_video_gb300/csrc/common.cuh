@@ -28,6 +28,27 @@ enum : int {
 // pipeline is stuck, and the kernel gives up instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
+// Index checks of the debug build (compiled with -DVCA_DEBUG), standing in
+// for a memory checker: an index that addresses memory and comes from data
+// (a cached permutation, a label) is tested against its array's extent
+// before use; one outside [0, n) records kStatBadArg in the status word and
+// the access is skipped (a read gives zeros).  Release builds compile the
+// test away.
+#ifdef VCA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool index_ok(long long i, long long n, const int* status) {
+  if constexpr (kDebugChecks) {
+    if (i < 0 || i >= n) {
+      atomicOr(const_cast<int*>(status), kStatBadArg);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -78,18 +99,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete, for at most kWaitLimitNs.  On
+// Wait for the phase of `parity` to complete, for at most `limit_ns`.  On
 // expiry, or if another warp of the CTA already gave up (abort flag), returns
 // false after recording the timeout in the device status word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((n & 15u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatTimeout);
         return false;
@@ -101,14 +122,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // The same bound, busy-polling without suspension: for the one thread whose
 // reaction time is on the critical path (the MMA issuer).
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, int* status) {
+                                               volatile int* abort_flag, int* status,
+                                               uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatTimeout);
         return false;

@@ -13,6 +13,65 @@ __global__ void expcast_kernel(const float* acc, const float* a, const float* b,
     out[i] = (uint8_t)expcast_code(acc[i], a[i], b[i]);
 }
 
+// The softmax's per-row byte step of the 8-bit attention kernel, one thread
+// per row of 128 scores: mask the keys at and past valid[r], Mn = max(M[r],
+// a[r] * rowmax), then the ExpCast bytes relative to Mn (the same device
+// functions the kernel calls).
+__global__ void __launch_bounds__(64) expcast_rows_kernel(const float* s, const float* a,
+                                                          const float* M, const int* valid,
+                                                          uint8_t* codes, float* Mn_out,
+                                                          size_t rows) {
+  for (size_t r = blockIdx.x * (size_t)blockDim.x + threadIdx.x; r < rows;
+       r += (size_t)gridDim.x * blockDim.x) {
+    uint32_t sv[128];
+#pragma unroll
+    for (int c = 0; c < 128; ++c) sv[c] = __float_as_uint(s[r * 128 + c]);
+    const int vl = valid[r];
+    if (vl < 128) mask_tail128(sv, vl);
+    const float ar = a[r];
+    const float Mn = fmaxf(M[r], ar * row_max128(sv));
+    uint32_t w[32];
+    expcast_row_bytes(sv, ar, Mn, w);
+    uint4* o = reinterpret_cast<uint4*>(codes + r * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    Mn_out[r] = Mn;
+  }
+}
+
+// Failure path of the bounded waits: one CTA whose two barriers are never
+// arrived at.  Warp 0 waits on barrier 0 with the limit `limit_ns` (mode 0:
+// the suspending wait, mode 1: the spinning wait of the MMA issuers) and,
+// when it gives up, records the timeout and raises the CTA's abort flag;
+// warp 1 waits on barrier 1 with the kernels' own one-second limit and must
+// leave through that flag.  out[w] = 1 if warp w's wait returned false,
+// out[2 + w] = its nanoseconds in the wait.  No copy is in flight.
+__global__ void __launch_bounds__(64) wait_timeout_kernel(int mode, uint64_t limit_ns, int* status,
+                                                          uint64_t* out) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const uint64_t t0 = globaltimer();
+  bool ok;
+  if (warp == 0)
+    ok = mode == 0 ? mbar_wait(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns)
+                   : mbar_wait_spin(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns);
+  else
+    ok = mbar_wait(smem_u32(&bars[1]), 0, &abort_flag, status);
+  const uint64_t t1 = globaltimer();
+  if (lane == 0) {
+    out[warp] = ok ? 0u : 1u;
+    out[2 + warp] = t1 - t0;
+  }
+}
+
 __global__ void encode_kernel(const float* x, uint8_t* e4, uint8_t* e2, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -219,6 +278,25 @@ extern "C" int vca_debug_expcast(const float* acc, const float* a, const float* 
   if (!acc || !a || !b || !out) return VCA_ERR_INVALID_ARG;
   int blocks = (int)std::min<size_t>((n + 255) / 256, 152 * 16);
   expcast_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(acc, a, b, out, n);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+extern "C" int vca_debug_expcast_rows(const float* s, const float* a, const float* M,
+                                      const int* valid, uint8_t* codes, float* Mn, size_t rows,
+                                      vca_stream_t stream) {
+  if (rows == 0) return VCA_OK;
+  if (!s || !a || !M || !valid || !codes || !Mn) return VCA_ERR_INVALID_ARG;
+  if (((uintptr_t)codes & 15u) || rows > ((size_t)1 << 24)) return VCA_ERR_INVALID_ARG;
+  const int blocks = (int)std::min<size_t>((rows + 63) / 64, 152 * 8);
+  expcast_rows_kernel<<<blocks, 64, 0, (cudaStream_t)stream>>>(s, a, M, valid, codes, Mn, rows);
+  return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
+}
+
+extern "C" int vca_debug_wait_timeout(int mode, uint64_t limit_ns, int* status, uint64_t* out,
+                                      vca_stream_t stream) {
+  if ((mode != 0 && mode != 1) || !status || !out) return VCA_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > vca::kWaitLimitNs / 10) return VCA_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(mode, limit_ns, status, out);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }
 

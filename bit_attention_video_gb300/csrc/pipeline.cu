@@ -116,21 +116,29 @@ int vca_pipeline_submit(vca_pipeline* p, const void* q_host, const void* k_host,
   const bool reused = i >= p->slots;
   // inputs: after step i - slots has finished reading the slot
   if (reused && cudaStreamWaitEvent(p->h2d, p->consumed[s], 0) != cudaSuccess) return VCA_ERR_CUDA;
+  // From the first copy on, a failure must not leave work in flight that
+  // still reads the caller's host buffers or the slot: wait for all of it.
+  auto fail = [&](int rc) {
+    cudaStreamSynchronize(p->h2d);
+    cudaStreamSynchronize(p->compute);
+    cudaStreamSynchronize(p->d2h);
+    return rc;
+  };
   const void* src[3] = {q_host, k_host, v_host};
   uint8_t* dst[3] = {dq, dk, dv};
   for (int t = 0; t < 3; ++t)
     if (cudaMemcpyAsync(dst[t], src[t], nbytes, cudaMemcpyHostToDevice, p->h2d) != cudaSuccess)
-      return VCA_ERR_CUDA;
-  if (cudaEventRecord(p->in_ready[s], p->h2d) != cudaSuccess) return VCA_ERR_CUDA;
+      return fail(VCA_ERR_CUDA);
+  if (cudaEventRecord(p->in_ready[s], p->h2d) != cudaSuccess) return fail(VCA_ERR_CUDA);
   // compute: once the inputs landed and step i - slots's O was read back
-  if (cudaStreamWaitEvent(p->compute, p->in_ready[s], 0) != cudaSuccess) return VCA_ERR_CUDA;
+  if (cudaStreamWaitEvent(p->compute, p->in_ready[s], 0) != cudaSuccess) return fail(VCA_ERR_CUDA);
   if (reused && cudaStreamWaitEvent(p->compute, p->d2h_done[s], 0) != cudaSuccess)
-    return VCA_ERR_CUDA;
+    return fail(VCA_ERR_CUDA);
   int rc = vca_vsmooth_prepare_ex(dq, dk, dv, p->B, p->H, p->N, p->d, p->k, reuse_perm, p->bits,
                                   iters, seed, flags & VCA_PREP_QK_HADAMARD, p->ws,
                                   p->state_bytes,
                                   (vca_stream_t)p->compute);
-  if (rc != VCA_OK) return rc;
+  if (rc != VCA_OK) return fail(rc);
   const vca_stream_t cs = (vca_stream_t)p->compute;
   if (p->bits == 4)
     rc = vca_attention_nvfp4(p->ws, p->state_bytes, p->B, p->H, p->N, p->d, dout, cs);
@@ -138,13 +146,13 @@ int vca_pipeline_submit(vca_pipeline* p, const void* q_host, const void* k_host,
     rc = vca_attention_fp8_exp(p->ws, p->state_bytes, p->B, p->H, p->N, p->d, dout, cs);
   else
     rc = vca_attention_fp8(p->ws, p->state_bytes, p->B, p->H, p->N, p->d, dout, cs);
-  if (rc != VCA_OK) return rc;
-  if (cudaEventRecord(p->consumed[s], p->compute) != cudaSuccess) return VCA_ERR_CUDA;
+  if (rc != VCA_OK) return fail(rc);
+  if (cudaEventRecord(p->consumed[s], p->compute) != cudaSuccess) return fail(VCA_ERR_CUDA);
   // read-back
-  if (cudaStreamWaitEvent(p->d2h, p->consumed[s], 0) != cudaSuccess) return VCA_ERR_CUDA;
+  if (cudaStreamWaitEvent(p->d2h, p->consumed[s], 0) != cudaSuccess) return fail(VCA_ERR_CUDA);
   if (cudaMemcpyAsync(o_host, dout, nbytes, cudaMemcpyDeviceToHost, p->d2h) != cudaSuccess)
-    return VCA_ERR_CUDA;
-  if (cudaEventRecord(p->d2h_done[s], p->d2h) != cudaSuccess) return VCA_ERR_CUDA;
+    return fail(VCA_ERR_CUDA);
+  if (cudaEventRecord(p->d2h_done[s], p->d2h) != cudaSuccess) return fail(VCA_ERR_CUDA);
   p->submitted = i + 1;
   if (step) *step = i;
   return VCA_OK;

@@ -667,8 +667,10 @@ __global__ void sort_hist_kernel(const int32_t* labels, int32_t* hist, int N, in
   for (int i = threadIdx.x; i < k; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const int t0 = ch * kSortChunk, t1 = min(N, t0 + kSortChunk);
-  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x)
-    atomicAdd(&h[labels[(size_t)bh * N + t]], 1);
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+    const int z = labels[(size_t)bh * N + t];
+    if (index_ok(z, k, status)) atomicAdd(&h[z], 1);
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < k; i += blockDim.x)
     hist[((size_t)bh * k + i) * nchunk + ch] = h[i];
@@ -715,8 +717,9 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* labels
     for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
     __syncthreads();
     const int t = r0 + threadIdx.x;
-    const bool valid = t < t1;
-    const int z = valid ? labels[(size_t)bh * N + t] : -1 - lane;  // unique per invalid lane
+    const int zt = t < t1 ? labels[(size_t)bh * N + t] : -1;
+    const bool valid = t < t1 && index_ok(zt, k, status);
+    const int z = valid ? zt : -1 - lane;  // unique per invalid lane
     const unsigned same = __match_any_sync(0xffffffffu, z);
     const int rank = __popc(same & ((1u << lane) - 1u));
     if (valid && rank == 0) wcnt[w][z] = __popc(same);
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t* labels
     if (valid) {
       int pos = base[z] + rank;
       for (int ww = 0; ww < w; ++ww) pos += wcnt[ww][z];
-      perm[(size_t)bh * N + pos] = t;
+      if (index_ok(pos, N, status)) perm[(size_t)bh * N + pos] = t;
     }
     __syncthreads();
     for (int m = threadIdx.x; m < k; m += blockDim.x) {
@@ -812,12 +815,12 @@ __device__ __forceinline__ void hadamard128_rows(float (&f)[8], int c8) {
 template <bool kRot>
 __device__ __forceinline__ void load_row8(const uint16_t* x, const int32_t* perm, bool centre,
                                           const float (&c)[8], int bh, int j, int u, int t,
-                                          int N, float (&v)[8]) {
+                                          int N, float (&v)[8], const int* status) {
   const int c8 = t % 16, row = j * 128 + u * 16 + t / 16;
 #pragma unroll
   for (int e = 0; e < 8; ++e) v[e] = 0.0f;
-  if (row < N) {
-    const int src = perm ? perm[(size_t)bh * N + row] : row;
+  const int src = row < N ? (perm ? perm[(size_t)bh * N + row] : row) : -1;
+  if (row < N && index_ok(src, N, status)) {
     const uint4 w = *reinterpret_cast<const uint4*>(x + ((size_t)bh * N + src) * 128 + c8 * 8);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -1012,8 +1015,8 @@ __global__ void __launch_bounds__(256, 4) quant_k8_rows_kernel(const uint16_t* k
   for (int u = 0; u < 8; ++u) {
     const int row = j * 128 + u * 16 + t / 16;
     valid[u] = row < N;
-    if (valid[u]) {
-      const int src = perm[(size_t)bh * N + row];
+    const int src = valid[u] ? perm[(size_t)bh * N + row] : -1;
+    if (valid[u] && index_ok(src, N, status)) {
       w[u] = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + src) * 128 + (t % 16) * 8);
     } else {
       w[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -1060,8 +1063,8 @@ __global__ void __launch_bounds__(256, 3) quant_k8_kernel(const uint16_t* k, con
   const int bh = blockIdx.y, j = blockIdx.x;
   const int r = threadIdx.x / 2, h = threadIdx.x % 2, row = j * 128 + r;
   float f[64];
-  if (row < N) {
-    const int src = perm[(size_t)bh * N + row];
+  const int src = row < N ? perm[(size_t)bh * N + row] : -1;
+  if (row < N && index_ok(src, N, status)) {
     load64(k + ((size_t)bh * N + src) * 128 + h * 64, f);
     const uint16_t* kb = kbar + (size_t)bh * 128 + h * 64;
     for (int i = 0; i < 64; ++i) f[i] = __fsub_rn(f[i], bf16_bits_to_f32(kb[i]));
@@ -1079,13 +1082,15 @@ __global__ void __launch_bounds__(256, 3) quant_k8_kernel(const uint16_t* k, con
 // Gather the 128 permuted rows of block j (bf16, zero rows past N) into shared
 // memory: 256 threads, coalesced 16-byte loads of whole 256-byte rows.
 __device__ __forceinline__ void gather_block(const uint16_t* v, const int32_t* perm, int bh, int j,
-                                             int N, uint16_t (*tile)[128]) {
+                                             int N, uint16_t (*tile)[128], const int* status) {
   for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
     const int r = i / 16, c16 = i % 16, row = j * 128 + r;
     uint4 w = make_uint4(0, 0, 0, 0);
-    if (row < N)
-      w = *reinterpret_cast<const uint4*>(
-          v + ((size_t)bh * N + perm[(size_t)bh * N + row]) * 128 + c16 * 8);
+    if (row < N) {
+      const int src = perm[(size_t)bh * N + row];
+      if (index_ok(src, N, status))
+        w = *reinterpret_cast<const uint4*>(v + ((size_t)bh * N + src) * 128 + c16 * 8);
+    }
     *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = w;
   }
 }
@@ -1102,7 +1107,7 @@ __global__ void __launch_bounds__(256) vpass1_kernel(const uint16_t* v, const in
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
   const int nj = min(128, N - j * 128);
-  gather_block(v, perm, bh, j, N, tile);
+  gather_block(v, perm, bh, j, N, tile, status);
   __syncthreads();
   if (c >= 128) return;
   float x[128];
@@ -1151,7 +1156,7 @@ __global__ void __launch_bounds__(256) vpass2_kernel(const uint16_t* v, const in
   const int bh = blockIdx.y, j = blockIdx.x;
   // threads t and t + 128 share channel c = t % 128, tokens 64 hh .. 64 hh + 63
   const int c = threadIdx.x % 128, hh = threadIdx.x / 128;
-  gather_block(v, perm, bh, j, N, tile);
+  gather_block(v, perm, bh, j, N, tile, status);
   __syncthreads();
   const size_t o = ((size_t)bh * nb + j) * 128 + c;
   const float mf = bf16_bits_to_f32(mu[o]);
@@ -1287,7 +1292,7 @@ __global__ void __launch_bounds__(256) rot_amax_rows_kernel(const uint16_t* x, c
 #pragma unroll 2
   for (int u = 0; u < 8; ++u) {
     float v[8];
-    load_row8<true>(x, nullptr, kbar != nullptr, c, bh, j, u, t, N, v);
+    load_row8<true>(x, nullptr, kbar != nullptr, c, bh, j, u, t, N, v, status);
 #pragma unroll
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
   }
@@ -1374,7 +1379,7 @@ __global__ void __launch_bounds__(256) quant_4_rows_kernel(const uint16_t* x, co
   for (int u = 0; u < 8; ++u) {
     const int m = u * 16 + t / 16, row = j * 128 + m;
     float v[8];
-    load_row8<kRot>(x, perm, kbar != nullptr, c, bh, j, u, t, N, v);
+    load_row8<kRot>(x, perm, kbar != nullptr, c, bh, j, u, t, N, v, status);
     uint32_t pk;
     const uint32_t sc = nvfp4_8_pair(v, g, pk);
     *reinterpret_cast<uint32_t*>(codes + ((size_t)bh * Npad + row) * 64 + c8 * 4) = pk;
@@ -1401,7 +1406,7 @@ __global__ void __launch_bounds__(256) vpass2_4_kernel(const uint16_t* v, const 
   __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  gather_block(v, perm, bh, j, N, tile);
+  gather_block(v, perm, bh, j, N, tile, status);
   __syncthreads();
   if (c >= 128) return;
   const size_t o = ((size_t)bh * nb + j) * 128 + c;
@@ -1670,6 +1675,13 @@ constexpr int kMaxDevices = 64;
 uint8_t* g_noalloc_ptr[kMaxDevices] = {};
 
 }  // namespace
+
+int* noalloc_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_noalloc_ptr[dev] ? reinterpret_cast<int*>(g_noalloc_ptr[dev] + kNaOffStatus) : nullptr;
+}
+
 }  // namespace vca
 
 extern "C" int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters,

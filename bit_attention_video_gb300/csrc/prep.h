@@ -50,6 +50,10 @@ int launch_attention_nvfp4(uint8_t* state, const vca_state_layout& L, int B, int
 int launch_attention_bf16(const void* q, const void* k, const void* v, int B, int H, int N,
                           void* o, int* status, cudaStream_t st);
 
+// The status word of vca_kmeans_permutation_noalloc's fixed scratch on the
+// current device, or nullptr if that entry point has not run on it yet.
+int* noalloc_status_word();
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 // 2-D tensor of `elem_bytes`-byte elements: inner extent `dim0`, `dim1` rows of
 // `row_bytes` bytes, box (box0, box1); `swizzle` = 128, 64 (bytes) or 0 (none).

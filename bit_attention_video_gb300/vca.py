@@ -7,6 +7,7 @@ loudly.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 
@@ -14,7 +15,12 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libvca.so")
+# the -DVCA_DEBUG build (index checks that record an error instead of an
+# out-of-bounds access), loaded beside the release build for tests
+LIB_DEBUG_PATH = os.path.join(_HERE, "_build_debug", "libvca.so")
 _lib = None
+_lib_debug = None
+_override = None
 
 VCA_OK = 0
 STATUS_NAMES = {0: "VCA_OK", -1: "VCA_ERR_INVALID_ARG", -2: "VCA_ERR_UNSUPPORTED",
@@ -45,56 +51,86 @@ class StateLayout(C.Structure):
 
 
 def lib():
-    """Load libvca.so (raises if it has not been built)."""
+    """Load libvca.so (raises if it has not been built).  Inside
+    ``debug_build()`` this is the VCA_DEBUG build instead."""
     global _lib
+    if _override is not None:
+        return _override
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: run bit_attention_video_gb300.build.build()")
-        L = C.CDLL(LIB_PATH)
-        P, I, S, U64 = C.c_void_p, C.c_int, C.c_size_t, C.c_uint64
-        L.vca_state_bytes.restype = S
-        L.vca_state_bytes.argtypes = [I] * 6
-        L.vca_state_layout_get.restype = I
-        L.vca_state_layout_get.argtypes = [I] * 6 + [C.POINTER(StateLayout)]
-        L.vca_vsmooth_prepare.restype = I
-        L.vca_vsmooth_prepare.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, P, S, P]
-        L.vca_vsmooth_prepare_ex.restype = I
-        L.vca_vsmooth_prepare_ex.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, C.c_uint, P,
-                                             S, P]
-        for fn in ("vca_attention_fp8", "vca_attention_fp8_exp", "vca_attention_nvfp4"):
-            getattr(L, fn).restype = I
-            getattr(L, fn).argtypes = [P, S, I, I, I, I, P, P]
-        L.vca_attention_bf16_ref.restype = I
-        L.vca_attention_bf16_ref.argtypes = [P, P, P, I, I, I, I, P, P, P]
-        L.vca_get_status.restype = I
-        L.vca_get_status.argtypes = [P, P, P]
-        L.vca_status_string.restype = C.c_char_p
-        L.vca_status_string.argtypes = [I]
-        L.vca_debug_expcast.restype = I
-        L.vca_debug_expcast.argtypes = [P, P, P, P, S, P]
-        L.vca_debug_encode.restype = I
-        L.vca_debug_encode.argtypes = [P, P, P, S, P]
-        L.vca_debug_mma.restype = I
-        L.vca_debug_mma.argtypes = [I, P, P, P, P]
-        L.vca_kmeans_permutation_noalloc.restype = I
-        L.vca_kmeans_permutation_noalloc.argtypes = [P, I, I, I, I, U64, I, I, I, P, P, P]
-        L.vca_pipeline_workspace_bytes.restype = S
-        L.vca_pipeline_workspace_bytes.argtypes = [I] * 7
-        L.vca_pipeline_create.restype = I
-        L.vca_pipeline_create.argtypes = [I] * 7 + [P, S, P, C.POINTER(C.c_void_p)]
-        L.vca_pipeline_submit.restype = I
-        L.vca_pipeline_submit.argtypes = [P, P, P, P, P, I, I, U64, C.c_uint,
-                                          C.POINTER(C.c_int64)]
-        L.vca_pipeline_wait.restype = I
-        L.vca_pipeline_wait.argtypes = [P, C.c_int64]
-        L.vca_pipeline_flush.restype = I
-        L.vca_pipeline_flush.argtypes = [P]
-        L.vca_pipeline_state.restype = P
-        L.vca_pipeline_state.argtypes = [P]
-        L.vca_pipeline_destroy.restype = I
-        L.vca_pipeline_destroy.argtypes = [P]
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def lib_debug():
+    """Load the VCA_DEBUG build (raises if it has not been built)."""
+    global _lib_debug
+    if _lib_debug is None:
+        _lib_debug = _load(LIB_DEBUG_PATH, "build(debug=True)")
+    return _lib_debug
+
+
+@contextlib.contextmanager
+def debug_build():
+    """Route every call of this module through the VCA_DEBUG build."""
+    global _override
+    prev, _override = _override, lib_debug()
+    try:
+        yield _override
+    finally:
+        _override = prev
+
+
+def _load(path, how="build()"):
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run bit_attention_video_gb300.build.{how}")
+    L = C.CDLL(path)
+    P, I, S, U64 = C.c_void_p, C.c_int, C.c_size_t, C.c_uint64
+    L.vca_state_bytes.restype = S
+    L.vca_state_bytes.argtypes = [I] * 6
+    L.vca_state_layout_get.restype = I
+    L.vca_state_layout_get.argtypes = [I] * 6 + [C.POINTER(StateLayout)]
+    L.vca_vsmooth_prepare.restype = I
+    L.vca_vsmooth_prepare.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, P, S, P]
+    L.vca_vsmooth_prepare_ex.restype = I
+    L.vca_vsmooth_prepare_ex.argtypes = [P, P, P, I, I, I, I, I, I, I, I, U64, C.c_uint, P,
+                                         S, P]
+    for fn in ("vca_attention_fp8", "vca_attention_fp8_exp", "vca_attention_nvfp4"):
+        getattr(L, fn).restype = I
+        getattr(L, fn).argtypes = [P, S, I, I, I, I, P, P]
+    L.vca_attention_bf16_ref.restype = I
+    L.vca_attention_bf16_ref.argtypes = [P, P, P, I, I, I, I, P, P, P]
+    L.vca_get_status.restype = I
+    L.vca_get_status.argtypes = [P, P, P]
+    L.vca_status_string.restype = C.c_char_p
+    L.vca_status_string.argtypes = [I]
+    L.vca_debug_expcast.restype = I
+    L.vca_debug_expcast.argtypes = [P, P, P, P, S, P]
+    L.vca_debug_expcast_rows.restype = I
+    L.vca_debug_expcast_rows.argtypes = [P, P, P, P, P, P, S, P]
+    L.vca_debug_encode.restype = I
+    L.vca_debug_encode.argtypes = [P, P, P, S, P]
+    L.vca_debug_mma.restype = I
+    L.vca_debug_mma.argtypes = [I, P, P, P, P]
+    L.vca_kmeans_permutation_noalloc.restype = I
+    L.vca_kmeans_permutation_noalloc.argtypes = [P, I, I, I, I, U64, I, I, I, P, P, P]
+    L.vca_pipeline_workspace_bytes.restype = S
+    L.vca_pipeline_workspace_bytes.argtypes = [I] * 7
+    L.vca_pipeline_create.restype = I
+    L.vca_pipeline_create.argtypes = [I] * 7 + [P, S, P, C.POINTER(C.c_void_p)]
+    L.vca_pipeline_submit.restype = I
+    L.vca_pipeline_submit.argtypes = [P, P, P, P, P, I, I, U64, C.c_uint,
+                                      C.POINTER(C.c_int64)]
+    L.vca_pipeline_wait.restype = I
+    L.vca_pipeline_wait.argtypes = [P, C.c_int64]
+    L.vca_pipeline_flush.restype = I
+    L.vca_pipeline_flush.argtypes = [P]
+    L.vca_pipeline_state.restype = P
+    L.vca_pipeline_state.argtypes = [P]
+    L.vca_pipeline_destroy.restype = I
+    L.vca_pipeline_destroy.argtypes = [P]
+    L.vca_debug_wait_timeout.restype = I
+    L.vca_debug_wait_timeout.argtypes = [I, U64, P, P, P]
+    return L
 
 
 def _check(fn, rc):
@@ -185,17 +221,40 @@ NOALLOC_MAX_TOKENS = 32768
 
 def kmeans_permutation_noalloc(v_head, k_clusters, labels, perm, iters=DEFAULT_ITERS,
                                seed=DEFAULT_SEED, b=0, h=0, H=1, stream=None):
-    """Grouping of one head without a state blob (scratch inside the library)."""
+    """Grouping of one head without a state blob (scratch inside the library).
+    Its device status word is read with noalloc_status()."""
     N, d = v_head.shape
+    if d != 128 or labels.numel() < N or perm.numel() < N:
+        raise VcaError("vca_kmeans_permutation_noalloc", -1 if d == 128 else -2)
     _check("vca_kmeans_permutation_noalloc", lib().vca_kmeans_permutation_noalloc(
         _dev(v_head, torch.bfloat16), N, d, k_clusters, iters, seed, b, h, H,
         _dev(labels, torch.int32), _dev(perm, torch.int32), _stream(stream)))
+
+
+def noalloc_status(stream=None) -> int:
+    """Synchronise the stream and read-and-clear the status word of the
+    allocation-free grouping call on the current device."""
+    return lib().vca_get_status(None, None, _stream(stream))
 
 
 def debug_expcast(acc, a, b, out, stream=None):
     _check("vca_debug_expcast", lib().vca_debug_expcast(
         _dev(acc, torch.float32), _dev(a, torch.float32), _dev(b, torch.float32),
         _dev(out, torch.uint8), acc.numel(), _stream(stream)))
+
+
+def debug_expcast_rows(s, a, M, valid, codes, Mn, stream=None):
+    """The attention softmax's per-row ExpCast step on rows of 128 scores."""
+    _check("vca_debug_expcast_rows", lib().vca_debug_expcast_rows(
+        _dev(s, torch.float32), _dev(a, torch.float32), _dev(M, torch.float32),
+        _dev(valid, torch.int32), _dev(codes, torch.uint8), _dev(Mn, torch.float32),
+        s.numel() // 128, _stream(stream)))
+
+
+def debug_wait_timeout(mode, limit_ns, status, out, stream=None):
+    """A CTA whose barriers are never arrived at (the bounded waits' failure path)."""
+    _check("vca_debug_wait_timeout", lib().vca_debug_wait_timeout(
+        mode, limit_ns, _dev(status, torch.int32), _dev(out, torch.int64), _stream(stream)))
 
 
 def debug_encode(x, out_e4m3, out_e2m1, stream=None):

@@ -202,8 +202,10 @@ int vca_attention_bf16_ref(const void* q, const void* k, const void* v, int B, i
                            int d, void* o, int* status, vca_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the status word of `state`
- * (or of the int32 at `status_word` when state is NULL).  Returns VCA_OK or the
- * first recorded error. */
+ * (or of the int32 at `status_word` when state is NULL; or, when both are
+ * NULL, the status word of vca_kmeans_permutation_noalloc's scratch on the
+ * current device, VCA_OK if that call has not run there).  Returns VCA_OK or
+ * the first recorded error. */
 int vca_get_status(void* state, int* status_word, vca_stream_t stream);
 
 /* Human-readable name of a vca_status value. */
@@ -220,7 +222,8 @@ const char* vca_status_string(int status);
  * vca_vsmooth_prepare stores as `labels` and `perm` for head (b, h) of an
  * H-head problem (same seed rule), without a state blob.
  *   v       bf16 [N, 128] device pointer (16-byte aligned), one head
- *   labels  int32 [N] device output, perm int32 [N] device output
+ *   labels  int32 [N] device output, perm int32 [N] device output (each at
+ *           least N entries: the kernels write N of each)
  *   N <= VCA_NOALLOC_MAX_TOKENS, else VCA_ERR_UNSUPPORTED (nothing launched).
  * Its scratch (about 4.3 MB) is a fixed array inside this library's device
  * image; every GPU that loads the library holds it until the process exits.
@@ -228,7 +231,12 @@ const char* vca_status_string(int status);
  * array's device address once (cudaGetSymbolAddress), so make that first
  * call before capturing any stream.  All calls share the one array: calls
  * whose execution overlaps on the GPU (other streams, other host threads)
- * race and must be serialised by the caller. */
+ * race and must be serialised by the caller.
+ * Device-side failures (for example, k distinct initial tokens that cannot be
+ * drawn) are recorded in a status word at the start of the array, which each
+ * call clears first; the call's later kernels then skip their work and labels
+ * and perm keep stale contents.  vca_get_status(NULL, NULL, stream) reads and
+ * clears that word on the current device. */
 int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k_clusters, int iters,
                                    uint64_t seed, int b, int h, int H, int32_t* labels,
                                    int32_t* perm, vca_stream_t stream);
@@ -293,7 +301,10 @@ int vca_pipeline_create(int B, int H, int N, int d, int k_clusters, int bits, in
 /* Enqueue one step.  reuse_perm, iters and seed as for vca_vsmooth_prepare_ex;
  * flags is VCA_PREP_QK_HADAMARD and/or VCA_PIPELINE_FP8_EXP.  On success *step
  * (may be NULL) receives the step number, 0, 1, 2, ... in submission order.
- * Does not block on the GPU. */
+ * Does not block on the GPU, except when a CUDA call fails after the step's
+ * copies were enqueued: then it waits for the pipeline's streams before
+ * returning the error, so the host buffers are free to reuse at once and the
+ * step's slot holds no work in flight (the step is not counted). */
 int vca_pipeline_submit(vca_pipeline* p, const void* q_host, const void* k_host,
                         const void* v_host, void* o_host, int reuse_perm, int iters,
                         uint64_t seed, unsigned flags, int64_t* step);
@@ -320,6 +331,30 @@ int vca_pipeline_destroy(vca_pipeline* p);
  * acc[i], b[i]))) (paper §3.3 Eq 7 in the single-FMA form). */
 int vca_debug_expcast(const float* acc, const float* a, const float* b, uint8_t* out, size_t n,
                       vca_stream_t stream);
+
+/* The per-row byte step of vca_attention_fp8's softmax, through the same
+ * device code (paper §3.3 Eq 7 and the running maximum of Eq 1): for each of
+ * `rows` rows of 128 fp32 scores s (raw QK^T accumulators, row-major), keys
+ * at and past valid[r] (1..128) are masked to -inf, Mn[r] = max(M[r],
+ * a[r] * max_c s[r][c]) (NaN scores ignored), and codes[r][c] is the ExpCast
+ * byte clip_[0,120](RNE(fma(a[r], s[r][c], 119.65f - Mn[r]))), evaluated in
+ * the kernel's paired 1/128-scaled form where that is exact and in the
+ * single-FMA form otherwise.  a[r] >= 0 as in the kernel (a product of
+ * positive scales).  codes: device, 16-byte aligned, rows x 128 bytes. */
+int vca_debug_expcast_rows(const float* s, const float* a, const float* M, const int* valid,
+                           uint8_t* codes, float* Mn, size_t rows, vca_stream_t stream);
+
+/* The failure path of the kernels' bounded waits, without a fault: one CTA
+ * whose barriers are never arrived at.  Its first warp waits with a limit of
+ * limit_ns (1 ns .. 100 ms; mode 0 the suspending wait, mode 1 the spinning
+ * wait of the MMA issuers), then records VCA_ERR_TIMEOUT's bit in the device
+ * int32 *status and raises the CTA's abort flag; its second warp waits with
+ * the kernels' own one-second limit and leaves through that flag.  out
+ * (device, 4 x uint64): per warp 1 if its wait gave up, then per warp the
+ * nanoseconds it waited.  vca_get_status(NULL, status, stream) then returns
+ * VCA_ERR_TIMEOUT. */
+int vca_debug_wait_timeout(int mode, uint64_t limit_ns, int* status, uint64_t* out,
+                           vca_stream_t stream);
 
 /* The device E4M3 and E2M1 encoders on n fp32 inputs (out_e2m1: one code per
  * byte, low nibble). */
