@@ -392,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(B_SFREE + X));
       if (j == nb - 1 && valid_last < 128) mask_tail128(s, valid_last);  // masked keys: byte 0
-      const float Mn = fmaxf(M, a * row_max128(s));
+      bool has_nan;
+      const float Mn = fmaxf(M, a * row_max128_flag(s, has_nan));
       const float alpha = ex2((M - Mn) * 0.125f);  // 0 on the first block
       // ExpCast bytes, four per 32-bit TMEM column (the A layout of the
       // product: byte k of column c is key 4c + k)
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[c / 4] = f32x4_to_e4m3x4(p0, p1, p2, p3);
         }
       } else {
-        expcast_row_bytes(s, a, Mn, w);
+        expcast_row_bytes(s, a, Mn, has_nan, w);
       }
       if (j > 0) {
         // the previous product read P^ and wrote the accumulator

@@ -84,6 +84,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase of `parity` (a few cycles; try_wait costs
+// over a hundred even on a completed phase).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // The same test, but the thread may be suspended up to `hint_ns` while the
 // phase is incomplete (no busy spinning).
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
@@ -117,6 +130,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+// mbar_wait for a phase that has usually completed already: the non-blocking
+// test first.
+__device__ __forceinline__ bool mbar_wait_likely(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort_flag, int* status) {
+  return mbar_test_wait(bar, parity) || mbar_wait(bar, parity, abort_flag, status);
 }
 
 // The same bound, busy-polling without suspension: for the one thread whose

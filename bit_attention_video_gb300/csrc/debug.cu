@@ -29,9 +29,10 @@ __global__ void __launch_bounds__(64) expcast_rows_kernel(const float* s, const 
     const int vl = valid[r];
     if (vl < 128) mask_tail128(sv, vl);
     const float ar = a[r];
-    const float Mn = fmaxf(M[r], ar * row_max128(sv));
+    bool has_nan;
+    const float Mn = fmaxf(M[r], ar * row_max128_flag(sv, has_nan));
     uint32_t w[32];
-    expcast_row_bytes(sv, ar, Mn, w);
+    expcast_row_bytes(sv, ar, Mn, has_nan, w);
     uint4* o = reinterpret_cast<uint4*>(codes + r * 128);
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);

@@ -18,37 +18,26 @@ __device__ __forceinline__ uint32_t expcast_code(float acc, float a, float b) {
   return __float_as_uint(__fadd_rn(t, 12582912.0f)) & 0xFFu;
 }
 
-// Kernel form on a pair: the FMA is evaluated on the 1/128-scaled operands
-// with saturation to [0, 1] (exact, scaling by a power of two commutes with
-// rounding), which clips below at 0; adding 1.5 * 2^16 rounds 128 t' to the
-// integer grid (ulp 2^-7), so the low byte of the sum is RNE(t).  The upper
-// clip at 120 can only act when |M| >= 2^20 (see expcast_fast_is_exact).
-// Returns the two fp32 bit patterns 0x47C00000 + code.
-__device__ __forceinline__ uint2 expcast_pair_bits(float acc0, float acc1, float a128,
-                                                   float b128) {
-  float t0, t1;
-  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(t0) : "f"(a128), "f"(acc0), "f"(b128));
-  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(t1) : "f"(a128), "f"(acc1), "f"(b128));
-  uint64_t in = ((uint64_t)__float_as_uint(t1) << 32) | __float_as_uint(t0), out;
-  const uint64_t magic = ((uint64_t)0x47C00000u << 32) | 0x47C00000u;  // 98304.0f x2
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(out) : "l"(in), "l"(magic));
-  return make_uint2((uint32_t)out, (uint32_t)(out >> 32));
-}
-
-// When the pair form gives exactly the reference form's byte, for scores with
-// a * acc <= M (M the running maximum, scaled by 8, log2 domain):
+// When the kernel form gives exactly the reference form's byte, for scores
+// with a * acc <= M (M the running maximum, scaled by 8, log2 domain; a > 0,
+// the product of positive scales):
 //   - |M| < 2^20: t = fma(a, acc, 119.65 - M) stays below 120.5 (the rounding
 //     of a * max and of 119.65 - M each add at most 2^-4), so the upper clip
 //     never acts;
-//   - a = 0 or a >= 2^-119: a * 2^-7 is exact (not subnormal).  (b * 2^-7 is
-//     always exact: 119.65 - M is 0 or at least 2^-18 in magnitude.)
+//   - a > 0: a masked key (acc = -inf) gives t = -inf, not NaN;
+//   - no score of the row is NaN (those rows take the reference form).
 __device__ __forceinline__ bool expcast_fast_is_exact(float M, float a) {
-  return fabsf(M) < 1048576.0f && (a == 0.0f || a >= 1.50463277e-36f /* 2^-119 */);
+  return fabsf(M) < 1048576.0f && a > 0.0f;
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
@@ -68,23 +57,58 @@ __device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
                fmaxf(m8[6], m8[7]));
 }
 
+// The same maximum, also telling whether the row holds a NaN score: one pass
+// of NaN-propagating max (the common case), the NaN-ignoring pass only for a
+// row that has one.
+__device__ __forceinline__ float row_max128_flag(const uint32_t (&s)[128], bool& has_nan) {
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    m8[i] = fmax3_nan(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]),
+                      __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      m8[i] = fmax3_nan(m8[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+  const float m = fmax3_nan(fmax3_nan(m8[0], m8[1], m8[2]), fmax3_nan(m8[3], m8[4], m8[5]),
+                            fmax3_nan(m8[6], m8[7], m8[7]));
+  has_nan = m != m;
+  return has_nan ? row_max128(s) : m;
+}
+
 // The ExpCast bytes of one row of a 128-key block relative to the running
 // maximum Mn (>= a * every score), four per word in the A-operand layout of
-// the value product (byte k of word c is key 4c + k).  The pair form when it
-// is exact, else the reference form.
+// the value product (byte k of word c is key 4c + k).
+// Kernel form, two scores per step: one paired FMA gives t = fma(a, acc,
+// 119.65 - Mn) exactly as the reference form does; multiplying by 2^-149
+// (paired) rounds t to the integer grid of fp32 subnormals with ties to even,
+// so the bits of the product are RNE(t) for 0 <= t < 2^23, and a sign bit
+// for t < 0 (or -inf); the saturating pack to unsigned bytes maps those to 0.
+// 1.5 instructions per score.  Rows the fast form is not exact for take the
+// reference form.
 __device__ __forceinline__ void expcast_row_bytes(const uint32_t (&s)[128], float a, float Mn,
-                                                  uint32_t (&w)[32]) {
+                                                  bool has_nan, uint32_t (&w)[32]) {
   const float b = kExpCastBias - Mn;
-  if (expcast_fast_is_exact(Mn, a)) {
-    const float a128 = a * 0.0078125f, b128 = b * 0.0078125f;
+  if (!has_nan && expcast_fast_is_exact(Mn, a)) {
+    const uint64_t a2 = ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
+    const uint64_t b2 = ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(b);
+    const uint64_t tiny = 0x0000000100000001ull;  // 2^-149, twice
 #pragma unroll
     for (int c = 0; c < 128; c += 4) {
-      const uint2 e0 = expcast_pair_bits(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), a128,
-                                         b128);
-      const uint2 e1 = expcast_pair_bits(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]),
-                                         a128, b128);
-      w[c / 4] = __byte_perm(__byte_perm(e0.x, e0.y, 0x0040), __byte_perm(e1.x, e1.y, 0x0040),
-                             0x5410);
+      uint64_t t01, t23, u01, u23;
+      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t01)
+          : "l"(((uint64_t)s[c + 1] << 32) | s[c]), "l"(a2), "l"(b2));
+      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t23)
+          : "l"(((uint64_t)s[c + 3] << 32) | s[c + 2]), "l"(a2), "l"(b2));
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(u01) : "l"(t01), "l"(tiny));
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(u23) : "l"(t23), "l"(tiny));
+      uint32_t hi, word;
+      asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(hi)
+          : "r"((uint32_t)(u23 >> 32)), "r"((uint32_t)u23), "r"(0u));
+      asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(word)
+          : "r"((uint32_t)(u01 >> 32)), "r"((uint32_t)u01), "r"(hi));
+      w[c / 4] = word;
     }
   } else {
 #pragma unroll

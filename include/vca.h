@@ -338,7 +338,8 @@ int vca_debug_expcast(const float* acc, const float* a, const float* b, uint8_t*
  * at and past valid[r] (1..128) are masked to -inf, Mn[r] = max(M[r],
  * a[r] * max_c s[r][c]) (NaN scores ignored), and codes[r][c] is the ExpCast
  * byte clip_[0,120](RNE(fma(a[r], s[r][c], 119.65f - Mn[r]))), evaluated in
- * the kernel's paired 1/128-scaled form where that is exact and in the
+ * the kernel's paired form (FMA, a multiply by 2^-149 that rounds onto the
+ * subnormal grid, a saturating byte pack) where that is exact and in the
  * single-FMA form otherwise.  a[r] >= 0 as in the kernel (a product of
  * positive scales).  codes: device, 16-byte aligned, rows x 128 bytes. */
 int vca_debug_expcast_rows(const float* s, const float* a, const float* M, const int* valid,

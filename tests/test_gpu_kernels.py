@@ -42,7 +42,7 @@ def _expcast_rows_inputs():
     running maximum M: random rows (first block, no rise, rise), exact
     rounding ties of the FMA, both clip ends, masked tails, NaN scores, |M|
     on both sides of 2^20 (where the kernel switches between its two forms)
-    and beyond, and subnormal a * 2^-7."""
+    and beyond, and tiny a."""
     rng = np.random.default_rng(31)
     R = 8192
     s = np.zeros((R, 128), np.float32)
@@ -86,7 +86,7 @@ def _expcast_rows_inputs():
         .astype(np.float32)
     s[r0:r1, 7] = (pick / a[r0:r1]).astype(np.float32)
     M[r0:r1] = np.where(rng.integers(0, 2, r1 - r0) == 0, -np.inf, pick).astype(np.float32)
-    # a below 2^-119 (a * 2^-7 subnormal: the single-FMA form) and just at it
+    # tiny a (scores near the fp32 maximum)
     r0, r1 = 6400, 6656
     a[r0:r1] = rng.choice(np.array([2.0 ** -121, 2.0 ** -120, 2.0 ** -119, 2.0 ** -118],
                                    np.float32), r1 - r0)
@@ -100,9 +100,10 @@ def _expcast_rows_inputs():
 
 def test_expcast_kernel_form_bit_exact(V, orc):
     """The softmax step the 8-bit attention kernel runs (paper §3.3 Eq 7 with
-    the running maximum of Eq 1): the paired 1/128-scaled FMA with the
-    1.5 x 2^16 rounding add where it is exact, the single-FMA form elsewhere,
-    byte for byte against the oracle's single-FMA fp32 form, on 2^20 scores."""
+    the running maximum of Eq 1): the paired FMA, the multiply by 2^-149 that
+    rounds onto the subnormal grid and the saturating byte pack where that is
+    exact, the single-FMA form elsewhere (NaN rows, |M| >= 2^20), byte for
+    byte against the oracle's single-FMA fp32 form, on 2^20 scores."""
     s, a, M, valid = _expcast_rows_inputs()
     R = s.shape[0]
     codes = torch.empty((R, 128), dtype=torch.uint8, device="cuda")
