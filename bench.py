@@ -56,9 +56,11 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             m = json.load(f)
+        load = m.get("clocks_under_load", {})
         return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
-                    bf16_sus=float(m["bf16_tflops_sustained"]), src="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+                    bf16_sus=float(m["bf16_tflops_sustained"]),
+                    sus_mhz=load.get("sm_mhz_median"), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sus_mhz=None, src="fallback")
 
 
 def attn_traffic(w):
@@ -123,6 +125,26 @@ def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
         total += BH * N * d * 2                 # V read by the feature pass
         total += BH * N * d * (1 + iters)       # int8 features: written once, read per iteration
         total += 4 * BH * N * iters             # labels written per iteration
+    return float(total)
+
+
+def vsmooth_min_bytes(w, iters: int, reuse: bool) -> float:
+    """The minimum DRAM bytes one V-Smooth preparation moves by the method
+    itself: read Q, K, V once; write the E4M3 codes of Q, K', R^T (or the
+    E2M1 codes and their scales); write the int8 features once and read them
+    once per Lloyd iteration; the permutation; block means and scales.  No
+    second read of V for the features and no per-iteration label writes (those
+    are this implementation's)."""
+    BH, N, d = w.B * w.H, w.N, w.d
+    nb = (N + 127) // 128
+    npad = nb * 128
+    total = 3 * BH * N * d * 2 + 4 * BH * N
+    if w.bits == 8:
+        total += 3 * BH * npad * d + BH * nb * d * (2 + 4) + BH * nb * 8
+    else:
+        total += 3 * BH * npad * d * (1 / 2 + 1 / 16) + BH * nb * d * 2
+    if not reuse:
+        total += BH * N * d * (1 + iters)
     return float(total)
 
 
@@ -220,20 +242,25 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    times, vals = [], []
+    times, vals, sampled = [], [], []
     for i in range(args.warmup + args.steps):
         r = cpu_oracle_sample(w, rows_per_head=8, seed_rows=i, iters=args.iters)
         if i >= args.warmup:
             vals.append(r["value"])
             times.append(r["t_step_s"])
+            sampled.append(r["t_prep_head_s"] + r["t_rows_s"])
         sample = r["sample"]
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": statistics.median(times) * 1e3, "higher_is_better": True,
+            "ms_per_step": statistics.median(times) * 1e3, "extrapolated": True,
+            "sample_s_per_step": statistics.median(sampled),
+            "ms_per_step_note": "extrapolated linearly from the timed sample (one head's "
+                                "preparation + 8 rows) to every head and row",
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k,
-                       "bits": w.bits},
+                       "iters": args.iters, "bits": w.bits, "grouping": "fresh"},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -346,6 +373,11 @@ def run_gpu(args, w):
     pk = peaks()
     tc_peak = pk["bf16_sus"] * PER_BF16[w.bits]
     pname = PEAK_NAME[w.bits]
+    # the sustained peak was measured at its own median clock; the same peak at
+    # this run's median clock (tensor throughput scales with the SM clock)
+    run_mhz = clocks.summary().get("sm_mhz")
+    tc_peak_at_run_clock = (tc_peak * run_mhz / pk["sus_mhz"]
+                            if run_mhz and pk.get("sus_mhz") else None)
 
     # End to end through the C ABI's host-buffer pipeline (vca_pipeline_*), as a
     # serving loop runs it: every step copies its Q, K, V from pinned host
@@ -445,12 +477,27 @@ def run_gpu(args, w):
         "vsmooth_gbs": vsmooth_bytes(w, grouping_iters(args), not groups(args))
         / (statistics.mean(prep_ms) * 1e-3) / 1e9,
         "vsmooth_bytes": vsmooth_bytes(w, grouping_iters(args), not groups(args)),
+        "vsmooth_min_bytes": vsmooth_min_bytes(w, grouping_iters(args), not groups(args)),
+        "vsmooth_gbs_min_bytes": vsmooth_min_bytes(w, grouping_iters(args), not groups(args))
+        / (statistics.mean(prep_ms) * 1e-3) / 1e9,
+        "vsmooth_frac_hbm_min_bytes": vsmooth_min_bytes(w, grouping_iters(args), not groups(args))
+        / (statistics.mean(prep_ms) * 1e-3) / 1e9 / pk["hbm"],
         "bf16_ref_ms": bf16_ms,
         "speedup_vs_bf16_ref": (bf16_ms / attn_avg) if bf16_ms else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": attn_tflops / tc_peak,
+                     "frac_at_run_clock": (attn_tflops / tc_peak_at_run_clock
+                                           if tc_peak_at_run_clock else None),
+                     "frac_note": "frac divides by the sustained peak measured at its own "
+                                  "median SM clock; frac_at_run_clock scales that peak to this "
+                                  "run's median SM clock (neither is tensor-pipe activity, "
+                                  "which ncu reports)",
                      # counters were taken on the ExpCast instantiation only
                      "traffic": None if exp_bytes(args) and w.bits == 8 else attn_traffic(w),
+                     "traffic_note": "DRAM read + write of one launch from one ncu capture of "
+                                     "the 16384-token, 24-head workload, scaled by token count; "
+                                     "part of O is still in L2 when that launch ends, so it "
+                                     "undercounts writes; null once the kernel source differs",
                      "kernel": ("attn_fp8_kernel<exp>" if exp_bytes(args) else "attn_fp8_kernel")
                      if w.bits == 8 else "attn_nvfp4_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
