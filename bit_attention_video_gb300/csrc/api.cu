@@ -51,7 +51,7 @@ int compute_layout(int B, int H, int N, int d, int k, int bits, vca_state_layout
   L->ksum = take(BH * nb * d * 4);
   L->vamax = take(BH * nb * d * 4);
   L->grid = take(BH * 8);
-  L->features = take(BH * N * d);
+  L->features = take(BH * N * d * 2);  // fp16 (k <= 128) or int8
   L->centroids = take(BH * k * d);
   L->sums = take(BH * k * d * 4 + BH * k * 4);
   L->total_bytes = (off + 1023) & ~uint64_t(1023);

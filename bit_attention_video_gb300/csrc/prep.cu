@@ -122,16 +122,17 @@ __global__ void head_amax_kernel(const uint16_t* v, uint32_t* amax_bits, size_t 
   if (threadIdx.x == 0) atomicMax(&amax_bits[bh], __float_as_uint(m));
 }
 
-// x = clamp(RNE(v / s), -127, 127), s = amax / 127 (1 if amax = 0).
+// x = clamp(RNE(v / s), -127, 127), s = amax / 127 (1 if amax = 0), stored
+// as int8 or, for the tensor-core Lloyd iterations, as fp16 (exact).
+template <bool kHalf>
 __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, float* grid_scale,
-                                int8_t* x, size_t per_head, const int* status) {
+                                void* x, size_t per_head, const int* status) {
   if (prep_skip(status)) return;
   const size_t bh = blockIdx.y;
   const float amax = __uint_as_float(amax_bits[bh]);
   const float s = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) grid_scale[bh] = s;
   const uint4* src = reinterpret_cast<const uint4*>(v + bh * per_head);
-  uint2* dst = reinterpret_cast<uint2*>(x + bh * per_head);
   const size_t n8 = per_head / 8;
   // RNE(v / s) from the bracketing products v rlo <= RN(v / s) <= v rhi (in
   // magnitude; rlo, rhi = (1/s)(1 -/+ 2^-20) rounded): integer rounding is
@@ -143,7 +144,7 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
        i += (size_t)gridDim.x * blockDim.x) {
     uint4 w = src[i];
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint32_t out[2] = {0, 0};
+    uint32_t out[2] = {0, 0}, out16[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const uint32_t bits = (e & 1) ? (ws[e / 2] & 0xFFFF0000u) : (ws[e / 2] << 16);
@@ -152,9 +153,19 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
       const float b = __fadd_rn(__fmul_rn(xv, rhi), 12582912.0f);
       int q = a == b ? (int)(__float_as_uint(a) - 0x4B400000u) : __float2int_rn(__fdiv_rn(xv, s));
       q = max(-127, min(127, q));
-      out[e / 4] |= ((uint32_t)(q & 0xFF)) << (8 * (e % 4));
+      if constexpr (kHalf) {
+        const uint32_t hb = __half_as_ushort(__int2half_rn(q));
+        out16[e / 2] |= hb << (16 * (e % 2));
+      } else {
+        out[e / 4] |= ((uint32_t)(q & 0xFF)) << (8 * (e % 4));
+      }
     }
-    dst[i] = make_uint2(out[0], out[1]);
+    if constexpr (kHalf)
+      reinterpret_cast<uint4*>(static_cast<uint16_t*>(x) + bh * per_head)[i] =
+          make_uint4(out16[0], out16[1], out16[2], out16[3]);
+    else
+      reinterpret_cast<uint2*>(static_cast<int8_t*>(x) + bh * per_head)[i] =
+          make_uint2(out[0], out[1]);
   }
 }
 
@@ -165,7 +176,8 @@ __global__ void features_kernel(const uint16_t* v, const uint32_t* amax_bits, fl
 // is accepted when no lane finds it (the draws and acceptances of a single
 // thread testing them in turn).  The k rows are then copied in 16-byte
 // chunks (d = 128).
-__global__ void kmeans_init_kernel(const int8_t* x, int8_t* cent, int32_t* sums, int32_t* counts,
+template <bool kHalf>
+__global__ void kmeans_init_kernel(const void* x, int8_t* cent, int32_t* sums, int32_t* counts,
                                    uint64_t seed, int N, int k, int d, int* status) {
   __shared__ int32_t idx[256];
   if (prep_skip(status)) return;
@@ -190,8 +202,34 @@ __global__ void kmeans_init_kernel(const int8_t* x, int8_t* cent, int32_t* sums,
   const int chunks = d / 16;
   for (int i = threadIdx.x; i < k * chunks; i += blockDim.x) {
     const int m = i / chunks, c16 = i % chunks;
-    reinterpret_cast<uint4*>(cent + ((size_t)bh * k + m) * d)[c16] =
-        reinterpret_cast<const uint4*>(x + ((size_t)bh * N + idx[m]) * d)[c16];
+    uint4 w;
+    if constexpr (kHalf) {
+      // 16 fp16 features (exact integers) -> 16 int8
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) +
+                                                        ((size_t)bh * N + idx[m]) * d) + 2 * c16;
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 in = src[h];
+        const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const uint32_t hw = iw[2 * e + f / 2] >> (16 * (f % 2));
+            const int q = __half2int_rn(__ushort_as_half((uint16_t)(hw & 0xFFFFu)));
+            word |= ((uint32_t)(q & 0xFF)) << (8 * f);
+          }
+          o[2 * h + e] = word;
+        }
+      }
+      w = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      w = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(x) +
+                                         ((size_t)bh * N + idx[m]) * d)[c16];
+    }
+    reinterpret_cast<uint4*>(cent + ((size_t)bh * k + m) * d)[c16] = w;
   }
   int4* s4 = reinterpret_cast<int4*>(sums + (size_t)bh * k * d);
   for (int i = threadIdx.x; i < k * d / 4; i += blockDim.x) s4[i] = make_int4(0, 0, 0, 0);
@@ -299,42 +337,44 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 
 // One Lloyd iteration on the tensor cores, for k <= 128.  grid (chunks, BH),
 // 256 threads; a CTA owns a run of 128-token tiles [tile0, tile0 + nt) of one
-// head.  With the int8 features and centroids held as fp16 (exact for
-// |x| <= 127) and fp32 accumulation (exact: every dot product and every
-// per-CTA sum of at most kPipeMaxTiles tiles stays below 2^24), per tile:
+// head.  The features are fp16 (the int8 grid values, exact) and accumulate
+// in fp32 (exact: every dot product and every per-CTA sum of at most
+// kPipeMaxTiles tiles stays below 2^24).  Per tile:
 //   D_a = X C^T       (M = 128 tokens, N = kpad centroids, K = 128 channels)
 //   label_t = argmin_m ||c_m||^2 - 2 D_a[t, m]  (lowest index on ties)
 //   D_u += X^T H      (M = 128 channels, N = kpad clusters, K = 128 tokens)
-// with H the one-hot label matrix.  The X tile is one shared-memory image:
-// K-major (128-byte swizzle) as the A operand of the first product and
-// MN-major as the A operand of the second; H is stored K-major as H^T.
-// Warp roles: warp 0 TMA producer of the int8 tiles (a ring of kPipeStages);
-// warp 1 MMA issuer and TMEM owner; warps 2, 3 and 8-11 convert each tile
-// to fp16 (two converter warps on the sub-partitions without the producer or
-// the issuer);
-// warps 4-7, one token row per thread (the TMEM lane), take each tile's
-// argmin and write its one-hot columns, so converting tile t+1 overlaps the
-// argmin of tile t.  H^T and D_a are double-buffered and X has nx = 3
-// buffers when shared memory allows (2 otherwise), so converting a tile waits
-// for the cluster-sum product of the tile nx before it.  The CTA's cluster sums
-// D_u and counts are added to the global sums once at the end.
-constexpr int kPipeStages = 3;
+// with H the one-hot label matrix.  The producer TMA-loads each fp16 tile as
+// two 128-byte-swizzled atoms (channels 0-63, 64-127) straight into one of nx
+// X buffers; that image is the K-major A operand of the first product and the
+// MN-major A operand of the second, and is reloaded once the second product
+// of its tile is done.  H is stored K-major as H^T.
+// Warp roles: warp 0 TMA producer; warp 1 MMA issuer and TMEM owner; warps
+// 4-7, one token row per thread (the TMEM lane), take each tile's argmin and
+// write its one-hot column while the products of the neighbouring tiles run.
+// H^T and D_a are double-buffered.  The CTA's cluster sums D_u and counts are
+// added to the global sums once at the end.
+// Each product is 8 instructions of K = 16 at N = kpad <= 128, which take
+// about as long as N = 144 ones: the tensor time of a tile is about 16 x 70
+// cycles, and at k = 64 the fp16 features read from HBM cost about as much.
 constexpr int kPipeMaxTiles = 1024;                   // 1024 * 128 * 127 < 2^24
-// shared memory: X bf16 nx x 32 KB | H^T bf16 2 x 32 KB | int8 tiles
-// kPipeStages x 16 KB | centroids bf16 kpad x 256 B
+constexpr int kPipeMaxX = 5;
+// shared memory: X fp16 nx x 32 KB | H^T fp16 2 x kpad x 256 B | centroids fp16
+// kpad x 256 B.  H^T[b] holds two 128-byte-swizzled atoms of kpad rows
+// (tokens 0-63, 64-127).
 constexpr uint32_t kPipeStaticSmem = 2048;            // the kernel's static shared memory, rounded up
 __host__ __device__ inline uint32_t kpipe_h(int nx) { return nx * 32768u; }
-__host__ __device__ inline uint32_t kpipe_s(int nx) { return kpipe_h(nx) + 65536u; }
-__host__ __device__ inline uint32_t kpipe_c(int nx) { return kpipe_s(nx) + kPipeStages * 16384u; }
-inline size_t kmeans_pipe_smem_bytes(int kpad, int nx) { return kpipe_c(nx) + (size_t)kpad * 256 + 1024; }
+__host__ __device__ inline uint32_t kpipe_c(int nx, int kpad) {
+  return kpipe_h(nx) + 2u * 256u * (uint32_t)kpad;
+}
+inline size_t kmeans_pipe_smem_bytes(int kpad, int nx) {
+  return kpipe_c(nx, kpad) + (size_t)kpad * 256 + 1024;
+}
 
 // barrier indices
-enum { KB_XFULL = 0, KB_XEMPTY = KB_XFULL + kPipeStages, KB_XREADY = KB_XEMPTY + kPipeStages,
-       KB_DA = KB_XREADY + 3, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
-       KB_CNT = KB_UDONE + 3, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
+enum { KB_XFULL = 0, KB_DA = KB_XFULL + kPipeMaxX, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
+       KB_CNT = KB_UDONE + kPipeMaxX, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
 
-constexpr int kPipeThreads = 384;
-constexpr int kConvThreads = 192;
+constexpr int kPipeThreads = 256;
 __global__ void __launch_bounds__(kPipeThreads, 1)
     kmeans_assign_pipe_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t* cent,
                               int32_t* labels, int32_t* sums, int32_t* counts, int N, int k,
@@ -355,7 +395,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   const int nt = min(tiles_per_cta, (N + 127) / 128 - tile0);
   if (nt <= 0) return;  // uniform over the CTA
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t kPX = 0, kPH = kpipe_h(nx), kPS = kpipe_s(nx), kPC = kpipe_c(nx);
+  const uint32_t kPX = 0, kPH = kpipe_h(nx), kPC = kpipe_c(nx, kpad);
+  const uint32_t hatom = (uint32_t)kpad * 128;    // one H^T atom: kpad rows x 128 B
+  const uint32_t hbuf = 2 * hatom;
   const uint32_t ncols = kpad <= 64 ? 256 : 512;
   const uint32_t col_u = kpad <= 64 ? 128 : 256;  // D_u; D_a[b] at b * kpad
   if (warp == 1) {
@@ -364,9 +406,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < KB_COUNT; ++i) {
-      const bool conv = i >= KB_XEMPTY && i < KB_XREADY + 3;
       const bool workers = (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
-      mbar_init(bar(i), conv ? kConvThreads : (workers ? 128 : 1));
+      mbar_init(bar(i), workers ? 128 : 1);
     }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -398,7 +439,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   }
   // both one-hot buffers start at zero; a worker later clears only the entry
   // it set two tiles before
-  for (int i = tid; i < 2 * 32768 / 16; i += kPipeThreads)
+  for (int i = tid; i < (int)(2 * hbuf / 16); i += kPipeThreads)
     reinterpret_cast<uint4*>(sm + kPH)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -411,37 +452,37 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     bool ok = true;
     int issued = 0;
     for (int t = 0; t < nt; ++t) {
-      const int s = t % kPipeStages;
-      if (t >= kPipeStages)
-        ok = mbar_wait(bar(KB_XEMPTY + s), ((t / kPipeStages) - 1) & 1, &abort_flag, status);
+      const int xi = t % nx;
+      // X[xi] was last read by the cluster-sum product of tile t - nx
+      if (t >= nx) ok = mbar_wait(bar(KB_UDONE + xi), ((t / nx) - 1) & 1, &abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) {
-        mbar_expect_tx(bar(KB_XFULL + s), 16384);
-        tma_load_2d(base + kPS + s * 16384, &tmX, bar(KB_XFULL + s), 0,
-                    bh * N + (tile0 + t) * 128);
+        const uint32_t xb = base + kPX + xi * 32768;
+        const int row = bh * N + (tile0 + t) * 128;
+        mbar_expect_tx(bar(KB_XFULL + xi), 32768);
+        tma_load_2d(xb, &tmX, bar(KB_XFULL + xi), 0, row);            // channels 0-63
+        tma_load_2d(xb + 16384, &tmX, bar(KB_XFULL + xi), 64, row);   // channels 64-127
       }
       ++issued;
     }
     if (lane == 0 && abort_flag) {
       // let the copies in flight land before the CTA exits
       const uint64_t t0 = globaltimer();
-      for (int t = max(0, issued - kPipeStages); t < issued; ++t) {
-        const int s = t % kPipeStages;
-        while (!mbar_try_wait(bar(KB_XFULL + s), (t / kPipeStages) & 1) &&
+      for (int t = max(0, issued - nx); t < issued; ++t)
+        while (!mbar_try_wait(bar(KB_XFULL + t % nx), (t / nx) & 1) &&
                globaltimer() - t0 < kWaitLimitNs) {
         }
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // per step t: assign(t) once tile t is converted, update(t-1) once its
+    // per step t: assign(t) once tile t has landed, update(t-1) once its
     // one-hot columns are written
     const uint32_t ia = idesc_f16(128, kpad), iu = idesc_f16(128, kpad, false, true);
     bool ok = true;
     for (int t = 0; t <= nt && ok; ++t) {
       if (t < nt) {
         const int b = t & 1, xi = t % nx;
-        ok = mbar_wait(bar(KB_XREADY + xi), (t / nx) & 1, &abort_flag, status);
+        ok = mbar_wait(bar(KB_XFULL + xi), (t / nx) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint32_t xb = base + kPX + xi * 32768;
@@ -459,11 +500,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         ok = mbar_wait(bar(KB_HREADY + b), (u >> 1) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t xb = base + kPX + (u % nx) * 32768, hb = base + kPH + b * 32768;
+        const uint32_t xb = base + kPX + (u % nx) * 32768, hb = base + kPH + b * hbuf;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_f16_ss_w(tmem + col_u, make_desc(xb + s * 2048, 16384, 1024, 2),
-                       desc_k_sw128(hb + (s / 4) * 16384 + (s % 4) * 32), iu, (u > 0 || s > 0));
+                       desc_k_sw128(hb + (s / 4) * hatom + (s % 4) * 32), iu, (u > 0 || s > 0));
         mma_commit_w(bar(KB_UDONE + u % nx));
       }
     }
@@ -472,46 +513,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar(KB_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
     }
-  } else if (warp >= 8 || warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ converters
-    // six warps: 2, 3 and 8-11.  Conversion step u (32 chunks, two rows)
-    // belongs to converter index u % 6; index 5 (warp 9, beside the MMA
-    // issuer) takes the fewest steps
-    const int ci = warp == 2 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 10 ? 3 : warp == 11 ? 4 : 5;
-    bool ok = true;
-    for (int t = 0; t < nt && ok; ++t) {
-      {
-        // convert tile t: int8 rows (no swizzle) -> fp16 K-major 128-byte
-        // swizzle (channels 0-63 and 64-127 in two 16 KB atoms)
-        const int s = t % kPipeStages, xi = t % nx;
-        ok = mbar_wait(bar(KB_XFULL + s), (t / kPipeStages) & 1, &abort_flag, status);
-        // X[xi] was last read by the cluster-sum product of tile t - nx
-        if (ok && t >= nx) ok = mbar_wait(bar(KB_UDONE + xi), ((t / nx) - 1) & 1, &abort_flag, status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint8_t* src = sm + kPS + s * 16384;
-        uint8_t* xb = sm + kPX + xi * 32768;
-        // one 16-byte chunk (8 channels) per thread and step: a warp covers
-        // two whole rows, so each group of 8 lanes reads 64 contiguous bytes
-        // and writes the 8 (swizzled) chunks of one 128-byte atom row:
-        // no shared-memory bank conflicts
-#pragma unroll
-        for (int n = 0; n < 11; ++n) {
-          const int u = ci + 6 * n;
-          if (u >= 64) break;
-          const int i = 32 * u + lane, r = i >> 4, c8 = i & 15;  // row r, channels 8 c8 ..
-          const uint2 in = *reinterpret_cast<const uint2*>(src + r * 128 + c8 * 8);
-          uint32_t w[4];
-          i8x4_to_f16x4(in.x, w[0], w[1]);
-          i8x4_to_f16x4(in.y, w[2], w[3]);
-          uint8_t* dst = xb + (c8 >> 3) * 16384 + r * 128;
-          *reinterpret_cast<uint4*>(dst + (((c8 & 7) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(KB_XEMPTY + s));
-        mbar_arrive(bar(KB_XREADY + xi));
-      }
-    }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ argmin workers
     const int wt = tid - 128, quarter = warp - 4;  // token row / cluster row = TMEM lane
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
@@ -583,11 +585,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           }
         }
         const int token = (tile0 + u) * 128 + wt;
-        uint8_t* hb = sm + kPH + b * 32768;
-        // H^T[m][token] at (token / 64) * 16 KB + m * 128 B, 16-byte chunk
+        uint8_t* hb = sm + kPH + b * hbuf;
+        // H^T[m][token] at (token / 64) * hatom + m * 128 B, 16-byte chunk
         // (token % 64) / 8 swizzled with m % 8, element token % 8
         auto hoff = [&](int m) {
-          return (wt / 64) * 16384 + m * 128 + ((((wt % 64) / 8) ^ (m & 7)) << 4) + (wt % 8) * 2;
+          return (wt / 64) * hatom + m * 128 + ((((wt % 64) / 8) ^ (m & 7)) << 4) + (wt % 8) * 2;
         };
         if (old_lab[b] >= 0) *reinterpret_cast<uint16_t*>(hb + hoff(old_lab[b])) = 0;
         old_lab[b] = -1;
@@ -1466,7 +1468,9 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
   if (a.reuse == 0 || a.reuse == 2) {
     uint32_t* amax_bits = reinterpret_cast<uint32_t*>(S + L.grid);
     float* gscale = reinterpret_cast<float*>(S + L.grid) + BH;
-    int8_t* x = reinterpret_cast<int8_t*>(S + L.features);
+    // features: fp16 for the tensor-core iterations (k <= 128), else int8
+    void* x = S + L.features;
+    const bool half_features = k <= 128;
     int8_t* cent = reinterpret_cast<int8_t*>(S + L.centroids);
     int32_t* sums = reinterpret_cast<int32_t*>(S + L.sums);
     int32_t* counts = sums + (size_t)BH * k * 128;
@@ -1476,20 +1480,30 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
     if (a.reuse == 2)
       kmeans_warm_kernel<<<BH, 128, 0, st>>>(amax_bits, gscale, cent, sums, counts, k, 128,
                                              status);
-    features_kernel<<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
-    if (a.reuse == 0)
-      kmeans_init_kernel<<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
+    if (half_features)
+      features_kernel<true><<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
+    else
+      features_kernel<false><<<dim3(ch, BH), 256, 0, st>>>(v, amax_bits, gscale, x, per_head, status);
+    if (a.reuse == 0) {
+      if (half_features)
+        kmeans_init_kernel<true><<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
+      else
+        kmeans_init_kernel<false><<<BH, 128, 0, st>>>(x, cent, sums, counts, a.seed, N, k, 128, status);
+    }
     if (k <= 128) {
       // tensor-core Lloyd iteration (the cluster-sum product has M = 128 rows):
       // each CTA takes a run of tiles of one head, runs sized to fill whole
       // waves of the SMs (and short enough for exact fp32 sums)
       const int kpad = (k + 15) / 16 * 16;
-      const int nx = kmeans_pipe_smem_bytes(kpad, 3) + kPipeStaticSmem <= 232448 ? 3 : 2;
+      int nx = kPipeMaxX;
+      while (nx > 2 && kmeans_pipe_smem_bytes(kpad, nx) + kPipeStaticSmem > 232448) --nx;
       const size_t psmem = kmeans_pipe_smem_bytes(kpad, nx);
       cudaFuncSetAttribute(kmeans_assign_pipe_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+      // fp16 rows of 128 channels; a box is one 128-byte swizzle atom
+      // (64 channels x 128 tokens)
       CUtensorMap tmx;
-      if (!make_tmap_2d(&tmx, x, 1, 128, (uint64_t)BH * N, 128, 128, 128, 0)) return VCA_ERR_CUDA;
+      if (!make_tmap_2d(&tmx, x, 2, 128, (uint64_t)BH * N, 256, 64, 128, 128)) return VCA_ERR_CUDA;
       int dev = 0, nsm = 152;
       cudaGetDevice(&dev);
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -1518,8 +1532,8 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
                            (int)asmem);
       const int tiles = (N + kAssignTokens - 1) / kAssignTokens;
       for (int it = 0; it < a.iters; ++it) {
-        kmeans_assign_kernel<<<dim3(tiles, BH), 256, asmem, st>>>(x, cent, labels, sums, counts,
-                                                                  N, k, groups, status);
+        kmeans_assign_kernel<<<dim3(tiles, BH), 256, asmem, st>>>(
+            static_cast<const int8_t*>(x), cent, labels, sums, counts, N, k, groups, status);
         kmeans_update_kernel<<<dim3(BH, k), 128, 0, st>>>(cent, sums, counts, k, status);
       }
     }
@@ -1726,8 +1740,8 @@ extern "C" int vca_kmeans_permutation_noalloc(const void* v, int N, int d, int k
   zero_kernel<<<1, 32, 0, st>>>(reinterpret_cast<uint32_t*>(S), 2 * 256 / 4);
   const int ch = grid_chunks(per_head / 8, 256 * 8, 1024);
   head_amax_kernel<<<dim3(ch, 1), 256, 0, st>>>(vv, amax_bits, per_head, status);
-  features_kernel<<<dim3(ch, 1), 256, 0, st>>>(vv, amax_bits, gscale, x, per_head, status);
-  kmeans_init_kernel<<<1, 128, 0, st>>>(x, cent, sums, counts, seed_mixed, N, k, 128, status);
+  features_kernel<false><<<dim3(ch, 1), 256, 0, st>>>(vv, amax_bits, gscale, x, per_head, status);
+  kmeans_init_kernel<false><<<1, 128, 0, st>>>(x, cent, sums, counts, seed_mixed, N, k, 128, status);
   const int groups = k <= 96 ? 2 : 1;
   const size_t asmem = assign_smem_bytes(k, groups);
   if (cudaFuncSetAttribute(kmeans_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -71,7 +71,7 @@ typedef struct {
   uint64_t perm;      /* int32 [BH][N]  pi: permuted row i holds source token perm[i] */
   uint64_t centroids; /* int8  [BH][k][d] centroids on the int8 feature grid */
   uint64_t grid;      /* fp32  [BH] per-head feature grid scale (and scratch) */
-  uint64_t features;  /* int8  [BH][N][d] k-means features (scratch) */
+  uint64_t features;  /* fp16 (k <= 128) or int8 [BH][N][d] k-means features (scratch) */
   uint64_t sums;      /* int32 [BH][k][d] + counts int32 [BH][k] (scratch) */
   uint64_t qhat;      /* e4m3  [BH][Npad][d] */
   uint64_t sq;        /* fp32  [BH][nb]    Q block scales */
