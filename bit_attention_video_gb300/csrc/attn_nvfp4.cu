@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pairs of keys: the exponent in fp32 (one paired FMA), then the
         // exponential, the block sum and the E2M1 cast in packed f16
         uint32_t hsum = 0u;   // f16x2 partial sums of q
-        uint32_t by[8];
+        uint32_t e[8];
         const uint64_t a2 = ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
         const uint64_t b2 = ((uint64_t)__float_as_uint(nbi) << 32) | __float_as_uint(nbi);
 #pragma unroll
@@ -429,21 +429,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t s2 = ((uint64_t)s[16 * i + c + 1] << 32) | s[16 * i + c];
           uint64_t x2;
           asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x2) : "l"(s2), "l"(a2), "l"(b2));
-          uint32_t h, e;
-          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(__uint_as_float((uint32_t)(x2 >> 32))),
+          uint32_t hx;
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hx) : "f"(__uint_as_float((uint32_t)(x2 >> 32))),
               "f"(__uint_as_float((uint32_t)x2)));
-          asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hsum) : "r"(hsum), "r"(e));
-          uint16_t bb;
-          asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f16x2 t, %1;\ncvt.u16.u8 %0, t;\n}"
-              : "=h"(bb) : "r"(e));
-          by[c / 2] = bb;
+          asm("ex2.approx.f16x2 %0, %1;" : "=r"(e[c / 2]) : "r"(hx));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hsum) : "r"(hsum), "r"(e[c / 2]));
         }
         const float hlo = __half2float(__ushort_as_half((uint16_t)(hsum & 0xFFFFu)));
         const float hhi = __half2float(__ushort_as_half((uint16_t)(hsum >> 16)));
         rs = fmaf(hlo + hhi, scv, rs);
-        pw[2 * i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
-        pw[2 * i + 1] = __byte_perm(__byte_perm(by[4], by[5], 0x0040), __byte_perm(by[6], by[7], 0x0040), 0x5410);
+        // the E2M1 casts, four code bytes (eight keys) per word, byte k =
+        // keys 2k, 2k+1 of the word
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          asm("{\n.reg .b8 t0, t1, t2, t3;\n"
+              "cvt.rn.satfinite.e2m1x2.f16x2 t0, %1;\ncvt.rn.satfinite.e2m1x2.f16x2 t1, %2;\n"
+              "cvt.rn.satfinite.e2m1x2.f16x2 t2, %3;\ncvt.rn.satfinite.e2m1x2.f16x2 t3, %4;\n"
+              "mov.b32 %0, {t0, t1, t2, t3};\n}"
+              : "=r"(pw[2 * i + h2])
+              : "r"(e[4 * h2]), "r"(e[4 * h2 + 1]), "r"(e[4 * h2 + 2]), "r"(e[4 * h2 + 3]));
       }
       if (j > 0) {
         ok = mbar_wait(bar(B_PVDONE + X), (j - 1) & 1, abort_flag, p.status);
