@@ -43,11 +43,11 @@ PEAK_NAME = {8: "fp8", 4: "fp4"}
 # O crosses DRAM once, so the figure scales with the token count.  It holds
 # only for the kernel source it was captured on.
 ATTN_TRAFFIC = {
-    8: dict(bytes=154.314496e6 + 67.907584e6, tokens=24 * 16384,
-            sources={"attn_fp8.cu": "a181635ea030b3dd1f424ac9bb7abc6b327b3a062847e1ca4d24c4f722499b3f",
-                     "expcast.cuh": "1f8628fe3b38fc742972d01508c454838b25acccb9f83fa6253f58019b6d08a1"}),
-    4: dict(bytes=88.149760e6 + 51.991040e6, tokens=24 * 16384,
-            sources={"attn_nvfp4.cu": "ad04e13f0a71a2630eb0b63400a2385b0e8906104c3ab5a438cace9cdb53c9ff"}),
+    8: dict(bytes=154.247680e6 + 67.890176e6, tokens=24 * 16384,
+            sources={"attn_fp8.cu": "2f036419ec42fd3faa6f78d86015fe4008ba4bc7a4b1fcda7bec3b44b4700084",
+                     "expcast.cuh": "7d3467df55804c0279e5a1512a3bb485fe81fd2e5f70119d7b8b69270ee0ff6c"}),
+    4: dict(bytes=88.151040e6 + 52.231680e6, tokens=24 * 16384,
+            sources={"attn_nvfp4.cu": "4a87e1ae3f6939e6de09578a5366f7fb535613942a85d8494fd36f66da224005"}),
 }
 
 
