@@ -63,6 +63,24 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sus_mhz=None, src="fallback")
 
 
+# The 4-bit attention is bound by its exponentials: one per score, an ex2 and a
+# lg2 per 16-score block scale, and one per row and key block for the rescale
+# factor.  The XU (MUFU) pipe retires 32 of them per clock per SM, in the fp32
+# and the packed f16 form alike (measured per-instruction costs).
+XU_OPS_PER_CLOCK_SM = 32
+
+
+def xu_roofline(w, attn_ms, sms, sm_max_mhz):
+    nb = (w.N + 127) // 128
+    ops = w.B * w.H * (w.N * w.N * (1 + 2 / 16) + w.N * nb)
+    peak = XU_OPS_PER_CLOCK_SM * sms * sm_max_mhz * 1e6 / 1e9
+    achieved = ops / (attn_ms * 1e-3) / 1e9
+    return {"bound": "alu", "unit": "Gop/s", "achieved": achieved, "peak": peak,
+            "frac": achieved / peak, "ops_per_launch": ops,
+            "note": f"MUFU operations of the softmax per launch / attention time; peak = "
+                    f"{XU_OPS_PER_CLOCK_SM} per clock per SM x {sms} SMs x {sm_max_mhz} MHz"}
+
+
 def attn_traffic(w):
     """Scaled DRAM traffic of one attention launch, or None if the kernel
     source differs from the one the counters were taken on."""
@@ -502,6 +520,10 @@ def run_gpu(args, w):
                      if w.bits == 8 else "attn_nvfp4_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
                                  f"{PER_BF16[w.bits]} (nominal {pname.upper()}:BF16 ratio)"},
+        "roofline_xu": (xu_roofline(w, attn_avg, torch.cuda.get_device_properties(dev)
+                                    .multi_processor_count,
+                                    clocks.summary().get("sm_max_mhz") or 2070.0)
+                        if w.bits == 4 else None),
         "e2e": ({"value": weak_value(world, w.flops, e2e_ms), "unit": "TFLOPS",
                  "ms_per_step": e2e_ms, "runs_ms_per_step": e2e_runs,
                  "h2d_bytes_per_step": 3 * nbytes,
