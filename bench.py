@@ -240,7 +240,9 @@ class OraclePool:
         import multiprocessing as mp
         import oracle
         oracle.build()          # once, before the workers load it
-        self.cores = max(1, min(os.cpu_count() or 1, heads))
+        avail = (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                 else (os.cpu_count() or 1))
+        self.cores = max(1, min(avail, heads))
         self.pool = mp.get_context("spawn").Pool(self.cores)
 
     def close(self):
