@@ -322,6 +322,74 @@ def weak_value(world: int, flops_per_rank: float, ms: float) -> float:
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+def nvfp4_companion(args, local):
+    """The 4-bit wan720p workload (B1 H40 N75600, NVFP4 operands) measured in
+    the same process after the main line: `args.steps` timed steps of a fresh
+    preparation and the NVFP4 attention, after `args.warmup` warm-up steps,
+    inputs resident in HBM."""
+    import torch
+    from bit_attention_video_gb300 import vca
+    w4 = synth.CONFIGS["wan720p_fp4"]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    shape = (w4.B, w4.H, w4.N, w4.d)
+    host = [torch.empty(shape, dtype=torch.bfloat16) for _ in range(3)]
+    synth.make_qkv(w4.B, w4.H, w4.N, w4.d, w4.clusters, w4.seed,
+                   out=tuple(h.view(torch.int16).numpy().view(np.uint16) for h in host))
+    q, k, v = (h.to(dev) for h in host)
+    del host
+    out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    att = vca.VCAttention(*shape, k_clusters=w4.k, bits=4, iters=args.iters, seed=0, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        att.prepare(q, k, v, reuse_perm=vca.PERM_FRESH)
+        if ev:
+            ev[1].record(stream)
+        vca.attention_nvfp4(att.state, shape, out)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(1 + args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if att.status() != 0:
+        raise RuntimeError(f"device status {att.status()} in the 4-bit companion")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if att.status() != 0:
+        raise RuntimeError(f"device status {att.status()} in the 4-bit companion")
+    ms_per_step = t0.elapsed_time(t1) / args.steps
+    attn_avg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    prep_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    attn_tflops = w4.flops / (attn_avg * 1e-3) / 1e12
+    pk = peaks()
+    tc_peak = pk["bf16_sus"] * PER_BF16[4]
+    cs = clocks.summary()
+    return {"workload": w4.name, "bits": 4, "grouping": "fresh", "iters": args.iters,
+            "steps": args.steps, "warmup": args.warmup,
+            "value": w4.flops / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOPS",
+            "ms_per_step": ms_per_step, "attention_ms": attn_avg, "vsmooth_ms": prep_avg,
+            "attention_tflops": attn_tflops,
+            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": attn_tflops / tc_peak,
+                         "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x 6"},
+            "roofline_xu": xu_roofline(w4, attn_avg,
+                                       torch.cuda.get_device_properties(dev).multi_processor_count,
+                                       cs.get("sm_max_mhz") or 2070.0),
+            "traffic": attn_traffic(w4),
+            "gpu_launches": launches_per_step(args.iters, False, 4) * args.steps,
+            "clocks": cs}
+
+
 def run_gpu(args, w):
     import torch
     from bit_attention_video_gb300 import vca
@@ -564,6 +632,11 @@ def run_gpu(args, w):
                      "rows": f"16 sampled query rows of heads {acc_heads} (batch 0), the last "
                              "timed step's output; exact attention in fp64 on the host inputs"},
     }
+    if world == 1 and w is synth.CONFIGS["wan720p"] and not args.no_nvfp4 and \
+            grouping_mode(args) == "fresh" and not args.qk_hadamard and not args.exp:
+        del q, k, v, out, host, out_host, att
+        torch.cuda.empty_cache()
+        line["nvfp4"] = nvfp4_companion(args, local)
     if dist:
         dist.barrier()
     if rank == 0 and not args.no_cpu_baseline:
@@ -600,6 +673,8 @@ def main():
     ap.add_argument("--skip-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-nvfp4", action="store_true",
+                    help="skip the 4-bit wan720p companion measurement of the default run")
     ap.add_argument("--e2e-steps", type=int, default=60,
                     help="steps per timed end-to-end run (the pipeline fills and drains once per run)")
     args = ap.parse_args()
