@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_w(bar(B_SFULL + X));
     };
     auto wait_sfree = [&](int X, int j) {
-      ok = mbar_wait(bar(B_SFREE + X), j & 1, abort_flag, p.status);
+      ok = mbar_wait_poll(bar(B_SFREE + X), j & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
     };
     if (ok) issue_s(0, 0, false);
@@ -258,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; ok && j + 1 < nb; ++j) {
       // the stage of block j+1 first (usually landed long before), so the wait
       // for the other tile is the last step before the product
-      ok = mbar_wait(bar(B_KVFULL + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag,
-                     p.status);
+      ok = mbar_wait_poll(bar(B_KVFULL + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag,
+                          p.status);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       wait_sfree(has_b ? 1 : 0, j);
       if (!ok) break;

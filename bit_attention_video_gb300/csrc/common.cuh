@@ -132,6 +132,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same bound, by non-blocking tests 32 ns apart: the waiting warp holds
+// no suspended try_wait.  The 4-bit attention's S issuer waits this way (its
+// sub-partition's softmax warps then lose fewer cycles to it).
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(32);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicOr(status, kStatTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // mbar_wait for a phase that has usually completed already: the non-blocking
 // test first.
 __device__ __forceinline__ bool mbar_wait_likely(uint32_t bar, uint32_t parity,

@@ -62,8 +62,9 @@ __global__ void __launch_bounds__(64) wait_timeout_kernel(int mode, uint64_t lim
   const uint64_t t0 = globaltimer();
   bool ok;
   if (warp == 0)
-    ok = mode == 0 ? mbar_wait(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns)
-                   : mbar_wait_spin(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns);
+    ok = mode == 0   ? mbar_wait(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns)
+         : mode == 1 ? mbar_wait_spin(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns)
+                     : mbar_wait_poll(smem_u32(&bars[0]), 0, &abort_flag, status, limit_ns);
   else
     ok = mbar_wait(smem_u32(&bars[1]), 0, &abort_flag, status);
   const uint64_t t1 = globaltimer();
@@ -295,7 +296,7 @@ extern "C" int vca_debug_expcast_rows(const float* s, const float* a, const floa
 
 extern "C" int vca_debug_wait_timeout(int mode, uint64_t limit_ns, int* status, uint64_t* out,
                                       vca_stream_t stream) {
-  if ((mode != 0 && mode != 1) || !status || !out) return VCA_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2 || !status || !out) return VCA_ERR_INVALID_ARG;
   if (limit_ns == 0 || limit_ns > vca::kWaitLimitNs / 10) return VCA_ERR_INVALID_ARG;
   wait_timeout_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(mode, limit_ns, status, out);
   return cudaGetLastError() == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;

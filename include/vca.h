@@ -348,7 +348,8 @@ int vca_debug_expcast_rows(const float* s, const float* a, const float* M, const
 /* The failure path of the kernels' bounded waits, without a fault: one CTA
  * whose barriers are never arrived at.  Its first warp waits with a limit of
  * limit_ns (1 ns .. 100 ms; mode 0 the suspending wait, mode 1 the spinning
- * wait of the MMA issuers), then records VCA_ERR_TIMEOUT's bit in the device
+ * wait of the MMA issuers, mode 2 the polled wait of the 4-bit S issuer), then
+ * records VCA_ERR_TIMEOUT's bit in the device
  * int32 *status and raises the CTA's abort flag; its second warp waits with
  * the kernels' own one-second limit and leaves through that flag.  out
  * (device, 4 x uint64): per warp 1 if its wait gave up, then per warp the

@@ -14,7 +14,7 @@ from gpu_util import bf16_f64, rel_l2, to_dev, to_np_u16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [0, 1], ids=["suspending", "spinning"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["suspending", "spinning", "polled"])
 def test_wait_gives_up_and_reports_timeout(orc, mode):
     from bit_attention_video_gb300 import vca
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -43,7 +43,7 @@ def test_wait_limit_arguments():
     from bit_attention_video_gb300 import vca
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.zeros(4, dtype=torch.int64, device="cuda")
-    for mode, limit in ((2, 1000), (0, 0), (0, 10 ** 9)):
+    for mode, limit in ((3, 1000), (-1, 1000), (0, 0), (0, 10 ** 9)):
         with pytest.raises(vca.VcaError):
             vca.debug_wait_timeout(mode, limit, status, out)
     assert np.all(out.cpu().numpy() == 0)
