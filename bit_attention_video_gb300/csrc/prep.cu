@@ -971,11 +971,18 @@ __global__ void __launch_bounds__(256) key_block_sum_kernel(const uint16_t* k, f
   __shared__ __align__(16) uint16_t tile[128][128];
   if (prep_skip(status)) return;
   const int bh = blockIdx.y, j = blockIdx.x, c = threadIdx.x;
-  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-    const int r = i / 16, c16 = i % 16, row = j * 128 + r;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (row < N) w = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + row) * 128 + c16 * 8);
-    *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = w;
+  {
+    // thread t: 16-byte chunk t % 16 of rows t / 16 + 16u, all eight loads in flight
+    const int c16 = threadIdx.x % 16, r0 = threadIdx.x / 16;
+    uint4 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int row = j * 128 + r0 + 16 * u;
+      w[u] = row < N ? *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + row) * 128 + c16 * 8)
+                     : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(&tile[r0 + 16 * u][c16 * 8]) = w[u];
   }
   __syncthreads();
   if (c >= 128) return;
@@ -1082,19 +1089,28 @@ __global__ void __launch_bounds__(256, 3) quant_k8_kernel(const uint16_t* k, con
 }
 
 // Gather the 128 permuted rows of block j (bf16, zero rows past N) into shared
-// memory: 256 threads, coalesced 16-byte loads of whole 256-byte rows.
+// memory, with the 256 threads the callers launch: thread t loads 16-byte
+// chunk t % 16 of rows t / 16 + 16u, u = 0..7, so each group of 16 lanes reads
+// one whole 256-byte row.  The eight indices are read first and the eight
+// rows next, so a thread has all its loads in flight at once.
 __device__ __forceinline__ void gather_block(const uint16_t* v, const int32_t* perm, int bh, int j,
                                              int N, uint16_t (*tile)[128], const int* status) {
-  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-    const int r = i / 16, c16 = i % 16, row = j * 128 + r;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (row < N) {
-      const int src = perm[(size_t)bh * N + row];
-      if (index_ok(src, N, status))
-        w = *reinterpret_cast<const uint4*>(v + ((size_t)bh * N + src) * 128 + c16 * 8);
-    }
-    *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = w;
+  const int c16 = threadIdx.x % 16, r0 = threadIdx.x / 16;
+  int src[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int row = j * 128 + r0 + 16 * u;
+    src[u] = row < N ? perm[(size_t)bh * N + row] : -1;
   }
+  uint4 w[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    w[u] = make_uint4(0, 0, 0, 0);
+    if (j * 128 + r0 + 16 * u < N && index_ok(src[u], N, status))
+      w[u] = *reinterpret_cast<const uint4*>(v + ((size_t)bh * N + src[u]) * 128 + c16 * 8);
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(&tile[r0 + 16 * u][c16 * 8]) = w[u];
 }
 
 // grid (nb, BH), 256 threads: block mean (Eq 4) of V' = V[pi]: fp32 tree sum
