@@ -125,11 +125,12 @@ def grouping_iters(args) -> int:
 
 
 def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
-    """Algorithmic DRAM bytes of one V-Smooth preparation: read Q, K, V (bf16)
-    once for the quantisers and V once more for the grouping features; write
-    the int8 features, read them once per Lloyd iteration; write the codes of
-    Q, K and R^T (E4M3, or E2M1 plus one UE4M3 scale per 16), the
-    permutation, the block means and the scales."""
+    """DRAM bytes this implementation's V-Smooth preparation moves: read Q, K,
+    V (bf16) once for the quantisers and V once more for the grouping
+    features; write the features (the int8 grid values, stored as fp16 for
+    k <= 128), read them once per Lloyd iteration; write the codes of Q, K and
+    R^T (E4M3, or E2M1 plus one UE4M3 scale per 16), the permutation, the
+    block means and the scales."""
     BH, N, d = w.B * w.H, w.N, w.d
     nb = (N + 127) // 128
     npad = nb * 128
@@ -141,7 +142,8 @@ def vsmooth_bytes(w, iters: int, reuse: bool) -> float:
     total += 4 * BH * N * 2                     # permutation: written, read by the gathers
     if not reuse:
         total += BH * N * d * 2                 # V read by the feature pass
-        total += BH * N * d * (1 + iters)       # int8 features: written once, read per iteration
+        feat = 2 if w.k <= 128 else 1           # fp16 or int8 features
+        total += BH * N * d * feat * (1 + iters)  # written once, read per iteration
         total += 4 * BH * N * iters             # labels written per iteration
     return float(total)
 
