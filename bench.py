@@ -495,11 +495,12 @@ def run_gpu(args, w):
     # Timed on the host clock from the first submit to the flush that returns
     # once the last O is in host memory.
     def time_e2e_pipelined():
-        pipe = vca.HostPipeline(*shape, k_clusters=w.k, bits=w.bits, slots=E2E_SLOTS,
+        slots = args.e2e_slots
+        pipe = vca.HostPipeline(*shape, k_clusters=w.k, bits=w.bits, slots=slots,
                                 iters=args.iters, seed=0, qk_hadamard=args.qk_hadamard,
                                 fp8_exp=exp_bytes(args), device=dev)
         outs_host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory()
-                     for _ in range(E2E_SLOTS)]
+                     for _ in range(slots)]
         first = [True]
 
         def run(n):
@@ -509,10 +510,10 @@ def run_gpu(args, w):
                 else:
                     kw = dict(reuse_perm=mode, iters=grouping_iters(args))
                 first[0] = False
-                pipe.submit(host[0], host[1], host[2], outs_host[i % E2E_SLOTS], **kw)
+                pipe.submit(host[0], host[1], host[2], outs_host[i % slots], **kw)
             pipe.flush()
 
-        run(E2E_SLOTS)
+        run(slots)
         if dist:
             dist.barrier()
         # three timed runs; the median is reported (the host's copy engines and
@@ -620,7 +621,7 @@ def run_gpu(args, w):
                  "d2h_bytes_per_step": nbytes,
                  "steps_per_run": args.e2e_steps,
                  "api": "vca_pipeline_submit / vca_pipeline_flush (host buffers)",
-                 "overlap": f"{E2E_SLOTS} device staging slots, one copy stream per direction: "
+                 "overlap": f"{args.e2e_slots} device staging slots, one copy stream per direction: "
                             "later steps' inputs and earlier steps' outputs move during the "
                             "compute; host clock from the first submit to the last O in host "
                             "memory"}
@@ -677,6 +678,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-nvfp4", action="store_true",
                     help="skip the 4-bit wan720p companion measurement of the default run")
+    ap.add_argument("--e2e-slots", type=int, default=E2E_SLOTS,
+                    help="device staging slots of the end-to-end pipeline")
     ap.add_argument("--e2e-steps", type=int, default=60,
                     help="steps per timed end-to-end run (the pipeline fills and drains once per run)")
     args = ap.parse_args()
