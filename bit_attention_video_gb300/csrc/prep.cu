@@ -351,27 +351,29 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const int8_t* x, con
 // Warp roles: warp 0 TMA producer; warp 1 MMA issuer and TMEM owner; warps
 // 4-7, one token row per thread (the TMEM lane), take each tile's argmin and
 // write its one-hot column while the products of the neighbouring tiles run.
-// H^T and D_a are double-buffered.  The CTA's cluster sums D_u and counts are
-// added to the global sums once at the end.
+// H^T and D_a are triple-buffered, and the cluster-sum product of tile t - 2
+// follows the assign product of tile t, so the argmin of a tile has two
+// products' time before its one-hot columns are needed.  The CTA's cluster
+// sums D_u and counts are added to the global sums once at the end.
 // Each product is 8 instructions of K = 16 at N = kpad <= 128, which take
 // about as long as N = 144 ones: the tensor time of a tile is about 16 x 70
 // cycles, and at k = 64 the fp16 features read from HBM cost about as much.
 constexpr int kPipeMaxTiles = 1024;                   // 1024 * 128 * 127 < 2^24
 constexpr int kPipeMaxX = 5;
-// shared memory: X fp16 nx x 32 KB | H^T fp16 2 x kpad x 256 B | centroids fp16
+// shared memory: X fp16 nx x 32 KB | H^T fp16 3 x kpad x 256 B | centroids fp16
 // kpad x 256 B.  H^T[b] holds two 128-byte-swizzled atoms of kpad rows
 // (tokens 0-63, 64-127).
 constexpr uint32_t kPipeStaticSmem = 2048;            // the kernel's static shared memory, rounded up
 __host__ __device__ inline uint32_t kpipe_h(int nx) { return nx * 32768u; }
 __host__ __device__ inline uint32_t kpipe_c(int nx, int kpad) {
-  return kpipe_h(nx) + 2u * 256u * (uint32_t)kpad;
+  return kpipe_h(nx) + 3u * 256u * (uint32_t)kpad;
 }
 inline size_t kmeans_pipe_smem_bytes(int kpad, int nx) {
   return kpipe_c(nx, kpad) + (size_t)kpad * 256 + 1024;
 }
 
 // barrier indices
-enum { KB_XFULL = 0, KB_DA = KB_XFULL + kPipeMaxX, KB_HREADY = KB_DA + 2, KB_UDONE = KB_HREADY + 2,
+enum { KB_XFULL = 0, KB_DA = KB_XFULL + kPipeMaxX, KB_HREADY = KB_DA + 3, KB_UDONE = KB_HREADY + 3,
        KB_CNT = KB_UDONE + kPipeMaxX, KB_DRAIN = KB_CNT + 1, KB_COUNT = KB_DRAIN + 1 };
 
 constexpr int kPipeThreads = 256;
@@ -398,15 +400,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   const uint32_t kPX = 0, kPH = kpipe_h(nx), kPC = kpipe_c(nx, kpad);
   const uint32_t hatom = (uint32_t)kpad * 128;    // one H^T atom: kpad rows x 128 B
   const uint32_t hbuf = 2 * hatom;
-  const uint32_t ncols = kpad <= 64 ? 256 : 512;
-  const uint32_t col_u = kpad <= 64 ? 128 : 256;  // D_u; D_a[b] at b * kpad
+  // D_a[b] at b * kpad (b < 3); the argmin reads max(64, kpad rounded up to
+  // 32) columns from there, so D_u starts past what D_a[2]'s reader touches
+  const uint32_t col_u = 2u * (uint32_t)kpad + (uint32_t)(kpad <= 64 ? 64 : (kpad + 31) / 32 * 32);
+  const uint32_t ncols = col_u + (uint32_t)kpad <= 256 ? 256 : 512;
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_slot), ncols);
     tmem_relinquish();
   }
   if (tid == 0) {
     for (int i = 0; i < KB_COUNT; ++i) {
-      const bool workers = (i >= KB_HREADY && i < KB_HREADY + 2) || i == KB_CNT;
+      const bool workers = (i >= KB_HREADY && i < KB_HREADY + 3) || i == KB_CNT;
       mbar_init(bar(i), workers ? 128 : 1);
     }
     abort_flag = 0;
@@ -437,9 +441,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
     cnorm[m] = (float)n2;
   }
-  // both one-hot buffers start at zero; a worker later clears only the entry
-  // it set two tiles before
-  for (int i = tid; i < (int)(2 * hbuf / 16); i += kPipeThreads)
+  // the one-hot buffers start at zero; a worker later clears only the entry
+  // it set three tiles before
+  for (int i = tid; i < (int)(3 * hbuf / 16); i += kPipeThreads)
     reinterpret_cast<uint4*>(sm + kPH)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -475,13 +479,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // per step t: assign(t) once tile t has landed, update(t-1) once its
+    // per step t: assign(t) once tile t has landed, update(t-2) once its
     // one-hot columns are written
     const uint32_t ia = idesc_f16(128, kpad), iu = idesc_f16(128, kpad, false, true);
     bool ok = true;
-    for (int t = 0; t <= nt && ok; ++t) {
+    for (int t = 0; t <= nt + 1 && ok; ++t) {
       if (t < nt) {
-        const int b = t & 1, xi = t % nx;
+        const int b = t % 3, xi = t % nx;
         ok = mbar_wait(bar(KB_XFULL + xi), (t / nx) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -495,9 +499,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
         mma_commit_w(bar(KB_DA + b));
       }
-      if (t >= 1) {
-        const int u = t - 1, b = u & 1;
-        ok = mbar_wait(bar(KB_HREADY + b), (u >> 1) & 1, &abort_flag, status);
+      if (t >= 2) {
+        const int u = t - 2, b = u % 3;
+        ok = mbar_wait(bar(KB_HREADY + b), (u / 3) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint32_t xb = base + kPX + (u % nx) * 32768, hb = base + kPH + b * hbuf;
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // ------------------------------------------------------------ argmin workers
     const int wt = tid - 128, quarter = warp - 4;  // token row / cluster row = TMEM lane
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-    int old_lab[2] = {-1, -1};  // the entry this thread set in H^T[b] two tiles before
+    int old_lab[3] = {-1, -1, -1};  // the entry this thread set in H^T[b] three tiles before
     bool ok = true;
     // used when kpad <= 64: ||c_m||^2 + 2^23 + 2^21 for a cluster, 1.5 * 2^24 past k
     float cn[64];
@@ -526,10 +530,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     for (int u = 0; u < nt && ok; ++u) {
       {
         // tile u: argmin of this token's row of D_a, then its one-hot column
-        const int b = u & 1;
-        ok = mbar_wait(bar(KB_DA + b), (u >> 1) & 1, &abort_flag, status);
-        // H^T[b] was last read by the cluster-sum product of tile u - 2
-        if (ok && u >= 2) ok = mbar_wait(bar(KB_UDONE + (u - 2) % nx), ((u - 2) / nx) & 1, &abort_flag, status);
+        const int b = u % 3;
+        ok = mbar_wait(bar(KB_DA + b), (u / 3) & 1, &abort_flag, status);
+        // H^T[b] was last read by the cluster-sum product of tile u - 3
+        if (ok && u >= 3) ok = mbar_wait(bar(KB_UDONE + (u - 3) % nx), ((u - 3) / nx) & 1, &abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint32_t trow = tmem + lanes + b * kpad;
@@ -1511,8 +1515,11 @@ static int launch_front(const PrepArgs& a, int bits, cudaStream_t st) {
       // each CTA takes a run of tiles of one head, runs sized to fill whole
       // waves of the SMs (and short enough for exact fp32 sums)
       const int kpad = (k + 15) / 16 * 16;
+      // nx >= 3: the producer reloads X[t % nx] after the cluster-sum product
+      // of tile t - nx, which is issued two steps after that tile's assign
       int nx = kPipeMaxX;
-      while (nx > 2 && kmeans_pipe_smem_bytes(kpad, nx) + kPipeStaticSmem > 232448) --nx;
+      while (nx > 3 && kmeans_pipe_smem_bytes(kpad, nx) + kPipeStaticSmem > 232448) --nx;
+      if (kmeans_pipe_smem_bytes(kpad, nx) + kPipeStaticSmem > 232448) return VCA_ERR_UNSUPPORTED;
       const size_t psmem = kmeans_pipe_smem_bytes(kpad, nx);
       cudaFuncSetAttribute(kmeans_assign_pipe_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
