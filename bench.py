@@ -38,15 +38,15 @@ NOMINAL_TFLOPS = {8: 4500.0, 4: 13500.0}
 PER_BF16 = {8: 2.0, 4: 6.0}
 PEAK_NAME = {8: "fp8", 4: "fp4"}
 
-# DRAM bytes (read + write) of one attention launch, from one ncu capture of
-# the 16384-token, 24-head workload per bit width.  Every row of Q, K, R and
-# O crosses DRAM once, so the figure scales with the token count.  It holds
-# only for the kernel source it was captured on.
+# DRAM bytes (read + write) of one attention launch, from one one-pass ncu
+# capture of the 75600-token, 40-head workload per bit width.  Every row of Q,
+# K, R and O crosses DRAM once, so the figure scales with the token count for
+# the other workloads.  It holds only for the kernel source it was captured on.
 ATTN_TRAFFIC = {
-    8: dict(bytes=154.247680e6 + 67.890176e6, tokens=24 * 16384,
+    8: dict(bytes=1194275072 + 746319872, tokens=40 * 75600,
             sources={"attn_fp8.cu": "2f036419ec42fd3faa6f78d86015fe4008ba4bc7a4b1fcda7bec3b44b4700084",
                      "expcast.cuh": "7d3467df55804c0279e5a1512a3bb485fe81fd2e5f70119d7b8b69270ee0ff6c"}),
-    4: dict(bytes=88.359936e6 + 51.569920e6, tokens=24 * 16384,
+    4: dict(bytes=686627328 + 731908096, tokens=40 * 75600,
             sources={"attn_nvfp4.cu": "d80ad69951fc79be70ea3d59423a2f53493376f3ae382a615a5b29bfd129a8c9"}),
 }
 
@@ -603,10 +603,11 @@ def run_gpu(args, w):
                                   "which ncu reports)",
                      # counters were taken on the ExpCast instantiation only
                      "traffic": None if exp_bytes(args) and w.bits == 8 else attn_traffic(w),
-                     "traffic_note": "DRAM read + write of one launch from one ncu capture of "
-                                     "the 16384-token, 24-head workload, scaled by token count; "
-                                     "part of O is still in L2 when that launch ends, so it "
-                                     "undercounts writes; null once the kernel source differs",
+                     "traffic_note": "DRAM read + write of one launch from a one-pass ncu "
+                                     "capture of the 75600-token, 40-head workload (scaled by "
+                                     "token count for other workloads); the last ~30 MB of O "
+                                     "are still in L2 when the launch ends; null once the "
+                                     "kernel source differs",
                      "kernel": ("attn_fp8_kernel<exp>" if exp_bytes(args) else "attn_fp8_kernel")
                      if w.bits == 8 else "attn_nvfp4_kernel",
                      "peak_src": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
