@@ -102,7 +102,9 @@ typedef struct {
 } vca_state_layout;
 
 /* Size in bytes of the state blob for this problem (0 if the arguments are
- * invalid).  The caller allocates it (any device allocation, 256-byte aligned). */
+ * invalid or unsupported: d != 128, bits not 8 or 4, k outside 1..min(256, N),
+ * B*H > 65535 or N > 2^24).  The caller allocates it (any device allocation,
+ * 256-byte aligned). */
 size_t vca_state_bytes(int B, int H, int N, int d, int k_clusters, int bits);
 
 /* Fill `out` with the offsets of the state blob's arrays.  Returns VCA_OK or
