@@ -12,8 +12,10 @@ int compute_layout(int B, int H, int N, int d, int k, int bits, vca_state_layout
   if (B < 1 || H < 1 || N < 1 || !L) return VCA_ERR_INVALID_ARG;
   if (d != 128 || (bits != 8 && bits != 4)) return VCA_ERR_UNSUPPORTED;
   if (k < 1 || k > 256 || k > N) return VCA_ERR_UNSUPPORTED;
-  // B*H is the y extent of the preparation's grids (at most 65535)
+  // B*H is the y extent of the preparation's grids (at most 65535); the TMA
+  // row coordinates and the token indices are 32-bit (B*H*Npad < 2^31)
   if ((int64_t)B * H > 65535 || N > (1 << 24)) return VCA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H * ((N + 127) / 128 * 128) >= (int64_t)1 << 31) return VCA_ERR_UNSUPPORTED;
   std::memset(L, 0, sizeof(*L));
   const uint64_t BH = (uint64_t)B * H, nb = (N + 127) / 128, Npad = nb * 128;
   uint64_t off = 0;

@@ -103,7 +103,7 @@ typedef struct {
 
 /* Size in bytes of the state blob for this problem (0 if the arguments are
  * invalid or unsupported: d != 128, bits not 8 or 4, k outside 1..min(256, N),
- * B*H > 65535 or N > 2^24).  The caller allocates it (any device allocation,
+ * B*H > 65535, N > 2^24, or B*H*Npad >= 2^31).  The caller allocates it (any device allocation,
  * 256-byte aligned). */
 size_t vca_state_bytes(int B, int H, int N, int d, int k_clusters, int bits);
 

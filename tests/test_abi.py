@@ -39,6 +39,7 @@ def test_state_bytes_and_layout(L):
     assert vca.state_bytes(1, 1, 100, 128, 8, 5) == 0      # bits
     assert vca.state_bytes(1, 65535, 128, 128, 8, 8) > 0   # B*H up to the grids' y extent
     assert vca.state_bytes(256, 256, 128, 128, 8, 8) == 0  # B*H = 65536
+    assert vca.state_bytes(1, 128, 1 << 24, 128, 8, 8) == 0  # B*H*Npad = 2^31
     a = vca.state_layout(2, 3, 1000, 128, 16, 8)
     b = vca.state_layout(2, 3, 1000, 128, 64, 8)
     # what the attention reads does not depend on k
