@@ -188,7 +188,7 @@ int vca_attention_nvfp4(void* state, size_t state_bytes, int B, int H, int N, in
 int vca_attention_bf16_ref(const void* q, const void* k, const void* v, int B, int H, int N,
                            int d, void* o, int* status, vca_stream_t stream) {
   if (B < 1 || H < 1 || N < 1) return VCA_ERR_INVALID_ARG;
-  if (d != 128) return VCA_ERR_UNSUPPORTED;
+  if (d != 128 || (int64_t)B * H > 65535 || N > (1 << 24)) return VCA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o) return VCA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return VCA_ERR_INVALID_ARG;
   return launch_attention_bf16(q, k, v, B, H, N, o, status, (cudaStream_t)stream);

@@ -198,7 +198,8 @@ int vca_attention_nvfp4(void* state, size_t state_bytes, int B, int H, int N, in
 
 /* BF16 reference attention on tcgen05 (the role BF16 FlashAttention-4 plays in
  * paper §4.1 "Baselines"): exact-max online softmax with an fp32 exponential,
- * bf16 probabilities.  q, k, v, o bf16 [B,H,N,d], device.  `status` is a
+ * bf16 probabilities.  q, k, v, o bf16 [B,H,N,d], device, 16-byte aligned;
+ * d = 128, B*H <= 65535, N <= 2^24 (else VCA_ERR_UNSUPPORTED).  `status` is a
  * device int32 that receives kernel-side failures (may be NULL). */
 int vca_attention_bf16_ref(const void* q, const void* k, const void* v, int B, int H, int N,
                            int d, void* o, int* status, vca_stream_t stream);
