@@ -47,7 +47,7 @@ ATTN_TRAFFIC = {
             sources={"attn_fp8.cu": "2f036419ec42fd3faa6f78d86015fe4008ba4bc7a4b1fcda7bec3b44b4700084",
                      "expcast.cuh": "7d3467df55804c0279e5a1512a3bb485fe81fd2e5f70119d7b8b69270ee0ff6c"}),
     4: dict(bytes=686627328 + 731908096, tokens=40 * 75600,
-            sources={"attn_nvfp4.cu": "d80ad69951fc79be70ea3d59423a2f53493376f3ae382a615a5b29bfd129a8c9"}),
+            sources={"attn_nvfp4.cu": "3feb0570546a161526cd829c996a17f8e1933dfbbf4b4961f7c9e4290ce76e10"}),
 }
 
 

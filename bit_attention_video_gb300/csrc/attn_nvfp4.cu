@@ -18,7 +18,7 @@
 //               scales of each block into tensor memory (tcgen05.cp), then
 //               issues S_A(j), S_B(j), S_A(j+1), ... each after the other tile
 //               loaded the shared S buffer; it polls its barriers (a
-//               non-blocking test every 32 ns), which holds back the softmax
+//               non-blocking test every ~128 ns), which holds back the softmax
 //               warps of its sub-partition less than a suspended wait
 //   warp 2      PV issuer: copies the R and P scales, issues PV_A(j), PV_B(j)
 //               and the mean products, and releases the stages

@@ -132,18 +132,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// The same bound, by non-blocking tests 32 ns apart: the waiting warp holds
+// The same bound, by non-blocking tests ~128 ns apart: the waiting warp holds
 // no suspended try_wait.  The 4-bit attention's S issuer waits this way (its
-// sub-partition's softmax warps then lose fewer cycles to it).
+// sub-partition's softmax warps then lose fewer cycles to it; 32-96 ns apart
+// the tests cost them more, 256 ns and longer delay the hand-over).
 __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, int* status,
                                                uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
-    __nanosleep(32);
+    __nanosleep(128);
     if (mbar_test_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {
+    if ((n & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
